@@ -1,0 +1,207 @@
+"""CPU oracle for the selective scan -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference`` legs of
+``bench.py`` may import this package. The library path (``selective_state_space_124_b300``) never
+imports, links or executes anything here, and this package imports nothing from it.
+
+Three independent evaluations of the same function live here:
+
+* ``Oracle.scan_fwd`` / ``Oracle.scan_step`` -- the plain sequential double-precision loop in
+  ``ssm_oracle.c`` (discretise, recur, read out, one time step after another; see that file's header
+  for the formula and the passage each step follows).
+* ``scan_1ss`` -- brute force through the explicit 1-semiseparable lower-triangular matrix of
+  "Mathematical Prerequisites for Mamba" s7 (h = L . diag(Bbar) . x with
+  L[t, j] = prod_{k=j+1..t} Abar_k), evaluated in numpy. It uses the closed form
+  prod_k exp(dt_k A) = exp(A * sum_k dt_k), so it shares no arithmetic path with the loop.
+* ``lti_conv`` -- the convolution view of a time-invariant system ("Understanding Mamba" s3.1,
+  Eqs. (4)-(5)): taps K_i = C . Abar^i . Bbar, y = x * K, through ``numpy.convolve``.
+
+All three run in float64. Discretisation names: ``"euler"`` (Bbar = delta * B, Abar kept exact) and
+``"zoh"`` (Bbar = (exp(delta A) - 1) / A * B).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "ssm_oracle.c")
+LIBPATH = os.path.join(_HERE, "liboracle.so")
+
+DISC = {"euler": 0, "zoh": 1}
+
+_build_lock = threading.Lock()
+
+
+def build(force: bool = False, src: str = SOURCE, out: str = LIBPATH) -> str:
+    """Compile ``ssm_oracle.c`` (plain C, OpenMP) into a shared library; returns its path."""
+    with _build_lock:
+        if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+            cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", out + ".tmp", src, "-lm"]
+            subprocess.run(cmd, check=True, capture_output=True)
+            os.replace(out + ".tmp", out)
+    return out
+
+
+def _as_input(a, f64: bool) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64 if f64 else np.float32)
+
+
+class Oracle:
+    """ctypes handle on one build of ``ssm_oracle.c`` (the default build, or a test's variant)."""
+
+    def __init__(self, libpath: str | None = None):
+        self.path = libpath or build()
+        lib = ctypes.CDLL(self.path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.oracle_scan_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, vp, i64, vp, vp]
+        lib.oracle_scan_fwd.restype = i32
+        lib.oracle_scan_step.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, i64, vp]
+        lib.oracle_scan_step.restype = i32
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = i32
+        self.lib = lib
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def scan_fwd(self, x, delta, A_log, B, C, disc="euler", h0=None, channels=None, f64=None):
+        """Prefill scan. x, delta: [batch, L, D]; B, C: [batch, L, N]; A_log: [D, N].
+
+        Returns (y, final_state) in float64. With ``channels`` None: y [batch, L, D] and
+        final_state [batch, D, N]; otherwise (a list of flat channel ids b*D + d) y [n_chan, L] and
+        final_state [n_chan, N]. ``h0`` (optional) is indexed like final_state. Inputs are passed as
+        float32 unless any of them is float64 (or ``f64`` is set), in which case all go as float64.
+        """
+        arrs = [np.asarray(a) for a in (x, delta, A_log, B, C)]
+        if f64 is None:
+            f64 = any(a.dtype == np.float64 for a in arrs)
+        x, delta, A_log, B, C = (_as_input(a, f64) for a in arrs)
+        batch, L, D = x.shape
+        N = A_log.shape[1]
+        assert delta.shape == x.shape and A_log.shape == (D, N)
+        assert B.shape == (batch, L, N) and C.shape == (batch, L, N)
+        chan = None if channels is None else np.ascontiguousarray(channels, dtype=np.int64)
+        n_chan = batch * D if chan is None else len(chan)
+        y = np.empty((n_chan, L), np.float64)
+        st = np.empty((n_chan, N), np.float64)
+        h0c = None
+        if h0 is not None:
+            h0c = np.ascontiguousarray(np.asarray(h0, np.float64).reshape(n_chan, N))
+        rc = self.lib.oracle_scan_fwd(
+            x.ctypes.data, delta.ctypes.data, A_log.ctypes.data, B.ctypes.data, C.ctypes.data,
+            None if h0c is None else h0c.ctypes.data, batch, L, D, N, DISC[disc], int(f64),
+            None if chan is None else chan.ctypes.data, n_chan, y.ctypes.data, st.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_scan_fwd rejected its arguments")
+        if chan is None:
+            return y.reshape(batch, D, L).transpose(0, 2, 1).copy(), st.reshape(batch, D, N)
+        return y, st
+
+    def scan_step(self, state, x_t, delta_t, A_log, B_t, C_t, disc="euler", channels=None, f64=None):
+        """One decode step. state: [batch, D, N] (or [n_chan, N] with ``channels``) float64;
+        x_t, delta_t: [batch, D]; B_t, C_t: [batch, N]. Returns (new_state, y_t)."""
+        arrs = [np.asarray(a) for a in (x_t, delta_t, A_log, B_t, C_t)]
+        if f64 is None:
+            f64 = any(a.dtype == np.float64 for a in arrs)
+        x_t, delta_t, A_log, B_t, C_t = (_as_input(a, f64) for a in arrs)
+        batch, D = x_t.shape
+        N = A_log.shape[1]
+        chan = None if channels is None else np.ascontiguousarray(channels, dtype=np.int64)
+        n_chan = batch * D if chan is None else len(chan)
+        st = np.array(state, dtype=np.float64, copy=True).reshape(n_chan, N)
+        st = np.ascontiguousarray(st)
+        y = np.empty(n_chan, np.float64)
+        rc = self.lib.oracle_scan_step(
+            st.ctypes.data, x_t.ctypes.data, delta_t.ctypes.data, A_log.ctypes.data, B_t.ctypes.data,
+            C_t.ctypes.data, batch, D, N, DISC[disc], int(f64),
+            None if chan is None else chan.ctypes.data, n_chan, y.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_scan_step rejected its arguments")
+        if chan is None:
+            return st.reshape(batch, D, N), y.reshape(batch, D)
+        return st, y
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default
+
+
+def scan_fwd(*args, **kw):
+    return default().scan_fwd(*args, **kw)
+
+
+def scan_step(*args, **kw):
+    return default().scan_step(*args, **kw)
+
+
+def num_threads() -> int:
+    return default().num_threads()
+
+
+def _discretise_np(dt, A, disc):
+    """Abar and Bbar/B for arrays dt (any shape) and A (broadcastable), numpy float64."""
+    z = dt * A
+    abar = np.exp(z)
+    if disc == "euler":
+        bfac = dt * np.ones_like(A)
+    else:
+        with np.errstate(divide="ignore", invalid="ignore"):
+            bfac = np.where(A == 0.0, dt * np.ones_like(A), np.expm1(z) / np.where(A == 0.0, 1.0, A))
+    return abar, bfac
+
+
+def scan_1ss(x, delta, A_log, B, C, disc="euler", h0=None):
+    """Brute force through the 1-semiseparable matrix ("Mathematical Prerequisites for Mamba" s6-s7).
+
+    For each (b, d, n): h[:, n] = M x with M[t, j] = exp(A_n (S_t - S_j)) Bbar_j for j <= t, where
+    S is the running sum of delta, plus exp(A_n S_t) h0 for a given initial state. y = sum_n C h.
+    O(L^2) per channel: tiny inputs only. Returns (y [batch, L, D], final_state [batch, D, N]).
+    """
+    x, delta, A_log, B, C = (np.asarray(a, np.float64) for a in (x, delta, A_log, B, C))
+    batch, L, D = x.shape
+    N = A_log.shape[1]
+    A = -np.exp(A_log)
+    y = np.zeros((batch, L, D))
+    hf = np.zeros((batch, D, N))
+    tri = np.tril(np.ones((L, L), bool))
+    for b in range(batch):
+        for d in range(D):
+            S = np.cumsum(delta[b, :, d])
+            H = np.zeros((L, N))
+            for n in range(N):
+                expo = A[d, n] * (S[:, None] - S[None, :])          # A_n * sum_{k=j+1..t} dt_k
+                Lmat = np.where(tri, np.exp(np.where(tri, expo, 0.0)), 0.0)
+                _, bfac = _discretise_np(delta[b, :, d], A[d, n], disc)
+                M = Lmat * (bfac * B[b, :, n])[None, :]             # L . diag(Bbar)
+                H[:, n] = M @ x[b, :, d]
+                if h0 is not None:
+                    H[:, n] += np.exp(A[d, n] * S) * np.asarray(h0, np.float64)[b, d, n]
+            y[b, :, d] = np.sum(C[b] * H, axis=1)
+            hf[b, d] = H[-1]
+    return y, hf
+
+
+def lti_conv(x, dt, A_log, B, C, disc="zoh"):
+    """Time-invariant special case through its convolution kernel ("Understanding Mamba" s3.1).
+
+    dt scalar, A_log [N], B and C [N] fixed for all t, x [L]. K_i = sum_n C_n Abar_n^i Bbar_n;
+    y = causal convolution of x with K (numpy.convolve). Returns (y [L], K [L]).
+    """
+    x = np.asarray(x, np.float64)
+    A = -np.exp(np.asarray(A_log, np.float64))
+    abar, bfac = _discretise_np(np.float64(dt), A, disc)
+    bbar = bfac * np.asarray(B, np.float64)
+    L = x.shape[0]
+    K = np.array([np.sum(np.asarray(C, np.float64) * abar ** i * bbar) for i in range(L)])
+    return np.convolve(x, K)[:L], K

@@ -1,0 +1,150 @@
+/*
+ * ssm_oracle.c -- plain, slow, sequential double-precision oracle for the selective scan.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the library path links, loads or calls this file.
+ * Only the tests, the smoke check and the benchmark's CPU-baseline leg use it.
+ *
+ * What it computes (one channel (b,d) at a time, time strictly sequential):
+ *
+ *   A[n]   = -exp(A_log[d,n])                     "Selective State Space Models" (aiwiki entry):
+ *                                                   A is stored as -exp(A_log), reference loop
+ *   abar   = exp(delta[b,t,d] * A[n])              "Understanding Mamba" s2.2, Eq. (2) (first half);
+ *                                                   the same exact Abar is kept in the first-order form
+ *                                                   ("State Space Models & Mamba" chapter, scalar
+ *                                                   selective recurrence and its code)
+ *   bbar*x = Euler: delta * B[b,t,n] * x[b,t,d]    aiwiki entry (dt * B, "what Mamba itself uses");
+ *                                                   chapter's Euler-simplified Bbar = delta * B
+ *            ZOH:   expm1(delta*A[n]) / A[n] * B[b,t,n] * x[b,t,d]
+ *                                                   "Understanding Mamba" s2.2 Eq. (2) second half,
+ *                                                   written as (Abar - 1)/A * B as in its discretize()
+ *                                                   example; "Mathematical Prerequisites for Mamba" s5
+ *            ZOH at A[n] == 0: delta * B * x       (continuous extension of (e^z - 1)/z -> 1; the
+ *                                                   chapter states the ZOH form only for A != 0)
+ *   h[n]   = abar * h[n] + bbar*x                  "Understanding Mamba" s2.3, Eq. (3)
+ *   y[b,t,d] = sum_n C[b,t,n] * h[n]               Eq. (3) readout with the feedthrough D set to 0
+ *                                                   (s2.1); aiwiki reference loop (state @ C_t)
+ *   h starts at 0 (or at h0 when given)             "Understanding Mamba" s3.1 (h_{-1} = 0)
+ *   final_state[b,d,:] = h after the last step      aiwiki reference loop keeps a [B, D, N] state
+ *
+ * Layouts (all row-major, dense): x, delta: [batch, L, D]; B, C: [batch, L, N]; A_log: [D, N];
+ * h0 / final_state: [batch, D, N] (or [n_chan, N] with a channel list, see below).
+ * Inputs arrive as float (fp32 values, or bf16 values widened exactly to fp32 by the caller) or,
+ * with is_f64 = 1, as double (used to feed the pages' worked examples exactly); every arithmetic
+ * step below runs in double.
+ *
+ * A channel list `chan` (flat ids b*D + d, n_chan of them) selects which channels to evaluate;
+ * chan == NULL means all batch*D channels in order. Outputs are per listed channel:
+ * y_out[k*L + t], state_out[k*N + n].
+ *
+ * Parallelism: OpenMP over independent channels only; each channel is one sequential loop.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_EULER = 0, ORACLE_ZOH = 1 };
+#define ORACLE_MAX_N 256
+
+/* Read element i of an input array that holds float (is_f64 == 0) or double (is_f64 == 1). */
+static double ld(const void *p, int64_t i, int is_f64)
+{
+    return is_f64 ? ((const double *)p)[i] : (double)((const float *)p)[i];
+}
+
+/* Discretised input term Bbar*x for one state entry (see the header comment for the sources). */
+static double oracle_bbar_x(double dlt, double a_n, double b_n, double x, int disc)
+{
+    if (disc == ORACLE_ZOH) {
+        if (a_n == 0.0) return dlt * b_n * x;      /* limit of expm1(z)/z -> 1 as A -> 0 */
+        return expm1(dlt * a_n) / a_n * b_n * x;
+    }
+    return dlt * b_n * x;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Prefill scan over whole sequences. Returns 0 on success, -1 on a bad argument.
+ * h0 may be NULL (zero initial state); when given it is indexed like state_out (per listed channel).
+ */
+int oracle_scan_fwd(const void *x, const void *delta, const void *A_log,
+                    const void *B, const void *C, const double *h0,
+                    int64_t batch, int64_t L, int64_t D, int64_t N, int disc, int is_f64,
+                    const int64_t *chan, int64_t n_chan,
+                    double *y_out, double *state_out)
+{
+    if (batch < 0 || L < 0 || D < 0 || N < 1 || N > ORACLE_MAX_N) return -1;
+    if (disc != ORACLE_EULER && disc != ORACLE_ZOH) return -1;
+    int64_t total = chan ? n_chan : batch * D;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t k = 0; k < total; ++k) {
+        int64_t flat = chan ? chan[k] : k;
+        if (flat < 0 || flat >= batch * D) { bad = 1; continue; }
+        int64_t b = flat / D, d = flat % D;
+        double h[ORACLE_MAX_N];
+        double A[ORACLE_MAX_N];
+        for (int64_t n = 0; n < N; ++n) {
+            A[n] = -exp(ld(A_log, d * N + n, is_f64));
+            h[n] = h0 ? h0[k * N + n] : 0.0;
+        }
+        for (int64_t t = 0; t < L; ++t) {
+            double xt = ld(x, (b * L + t) * D + d, is_f64);
+            double dt = ld(delta, (b * L + t) * D + d, is_f64);
+            int64_t bc = (b * L + t) * N;
+            double yt = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double abar = exp(dt * A[n]);
+                h[n] = abar * h[n] + oracle_bbar_x(dt, A[n], ld(B, bc + n, is_f64), xt, disc);
+                yt += ld(C, bc + n, is_f64) * h[n];
+            }
+            y_out[k * L + t] = yt;
+        }
+        for (int64_t n = 0; n < N; ++n) state_out[k * N + n] = h[n];
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * One recurrent decode step ("Understanding Mamba" s3.2 / s10.1: the same Eq. (3) body applied to a
+ * carried state). state: [n_chan, N] doubles, updated in place; x_t, delta_t: [batch, D];
+ * B_t, C_t: [batch, N]; y_t: [n_chan].
+ */
+int oracle_scan_step(double *state, const void *x_t, const void *delta_t, const void *A_log,
+                     const void *B_t, const void *C_t,
+                     int64_t batch, int64_t D, int64_t N, int disc, int is_f64,
+                     const int64_t *chan, int64_t n_chan, double *y_t)
+{
+    if (batch < 0 || D < 0 || N < 1 || N > ORACLE_MAX_N) return -1;
+    if (disc != ORACLE_EULER && disc != ORACLE_ZOH) return -1;
+    int64_t total = chan ? n_chan : batch * D;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t k = 0; k < total; ++k) {
+        int64_t flat = chan ? chan[k] : k;
+        if (flat < 0 || flat >= batch * D) { bad = 1; continue; }
+        int64_t b = flat / D, d = flat % D;
+        double xt = ld(x_t, b * D + d, is_f64);
+        double dt = ld(delta_t, b * D + d, is_f64);
+        double yt = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double A = -exp(ld(A_log, d * N + n, is_f64));
+            double abar = exp(dt * A);
+            double hn = abar * state[k * N + n] + oracle_bbar_x(dt, A, ld(B_t, b * N + n, is_f64), xt, disc);
+            state[k * N + n] = hn;
+            yt += ld(C_t, b * N + n, is_f64) * hn;
+        }
+        y_t[k] = yt;
+    }
+    return bad ? -1 : 0;
+}

@@ -1,0 +1,67 @@
+"""Planted mistakes in the oracle must each fail at least one pin.
+
+Each case rewrites one spot of ssm_oracle.c (a dropped term, a wrong sign, a wrong index, a swapped
+operand ...), compiles that variant into a temporary directory and runs every pin against it. The real
+oracle source is never modified.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_PINS
+
+MUTANTS = {
+    "drop_input_term": ("h[n] = abar * h[n] + oracle_bbar_x(dt, A[n], ld(B, bc + n, is_f64), xt, disc);",
+                        "h[n] = abar * h[n];"),
+    "A_positive": ("A[n] = -exp(ld(A_log, d * N + n, is_f64));", "A[n] = exp(ld(A_log, d * N + n, is_f64));"),
+    "A_log_transposed": ("A[n] = -exp(ld(A_log, d * N + n, is_f64));", "A[n] = -exp(ld(A_log, n * D + d, is_f64));"),
+    "readout_before_update": (
+        "                h[n] = abar * h[n] + oracle_bbar_x(dt, A[n], ld(B, bc + n, is_f64), xt, disc);\n"
+        "                yt += ld(C, bc + n, is_f64) * h[n];",
+        "                yt += ld(C, bc + n, is_f64) * h[n];\n"
+        "                h[n] = abar * h[n] + oracle_bbar_x(dt, A[n], ld(B, bc + n, is_f64), xt, disc);"),
+    "zoh_as_euler": ("if (disc == ORACLE_ZOH) {", "if (0) {"),
+    "euler_as_zoh": ("    return dlt * b_n * x;\n}", "    return expm1(dlt * a_n) / a_n * b_n * x;\n}"),
+    "zoh_missing_divide": ("return expm1(dlt * a_n) / a_n * b_n * x;", "return expm1(dlt * a_n) * b_n * x;"),
+    "zoh_exp_not_expm1": ("return expm1(dlt * a_n) / a_n * b_n * x;", "return exp(dlt * a_n) / a_n * b_n * x;"),
+    "B_from_C": ("oracle_bbar_x(dt, A[n], ld(B, bc + n, is_f64), xt, disc);",
+                 "oracle_bbar_x(dt, A[n], ld(C, bc + n, is_f64), xt, disc);"),
+    "BC_lag_one_step": ("int64_t bc = (b * L + t) * N;", "int64_t bc = (b * L + (t > 0 ? t - 1 : 0)) * N;"),
+    "x_delta_swapped": ("double xt = ld(x, (b * L + t) * D + d, is_f64);",
+                        "double xt = ld(delta, (b * L + t) * D + d, is_f64);"),
+    "abar_without_A": ("double abar = exp(dt * A[n]);", "double abar = exp(-dt);"),
+    "h0_ignored": ("h[n] = h0 ? h0[k * N + n] : 0.0;", "h[n] = 0.0;"),
+    "step_drops_decay": ("double hn = abar * state[k * N + n] +", "double hn = state[k * N + n] +"),
+    "step_reads_old_state": (
+        "            state[k * N + n] = hn;\n            yt += ld(C_t, b * N + n, is_f64) * hn;",
+        "            yt += ld(C_t, b * N + n, is_f64) * state[k * N + n];\n            state[k * N + n] = hn;"),
+    "channel_index_swapped": ("int64_t b = flat / D, d = flat % D;\n        double h[",
+                              "int64_t d = flat / D, b = flat % D;\n        double h["),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, 1)
+    path = tmp_path / "mut.c"
+    path.write_text(mutated)
+    lib = str(tmp_path / f"liboracle_{name}.so")
+    subprocess.run(["gcc", "-O1", "-fopenmp", "-fPIC", "-shared", "-o", lib, str(path), "-lm"], check=True)
+    mut = oracle.Oracle(lib)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(mut)
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake {name}"
+
+
+def test_real_oracle_passes_every_pin(orc):
+    for pin in ALL_PINS:
+        pin(orc)
