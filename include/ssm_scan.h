@@ -1,0 +1,102 @@
+/*
+ * ssm_scan.h -- C ABI of the B300 (sm_103a) selective-scan library, libssm_scan.so.
+ *
+ * The operation (Mamba's selective scan; "Understanding Mamba" s2.2-s2.3, Eqs. (2)-(3); the aiwiki
+ * "Selective State Space Models" reference loop for shapes and A = -exp(A_log)):
+ *
+ *   for every batch element b and channel d, with A[n] = -exp(A_log[d, n]) and h = h0[b, d, :] (or 0):
+ *     for t = 0 .. L-1, for n = 0 .. N-1:
+ *       Abar   = exp(delta[b,t,d] * A[n])
+ *       Bbar x = delta[b,t,d] * B[b,t,n] * x[b,t,d]                          (SSM_DISC_EULER)
+ *              = (exp(delta[b,t,d] A[n]) - 1) / A[n] * B[b,t,n] * x[b,t,d]   (SSM_DISC_ZOH;
+ *                                                     delta * B * x where A[n] == 0)
+ *       h[n]   = Abar * h[n] + Bbar x
+ *     y[b,t,d] = sum_n C[b,t,n] * h[n]                   (no feedthrough term, no gate)
+ *   final_state[b, d, :] = h after the last step.
+ *
+ * The first-order (Euler) input term keeps the exact Abar, as the pages' scalar recurrence and the
+ * aiwiki reference loop do ("State Space Models & Mamba" chapter; aiwiki entry: delta*B "is what Mamba
+ * itself uses"). delta is taken as given (already made positive upstream; no softplus inside).
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer is DEVICE memory of the current CUDA device, owned by the caller. The library
+ *    allocates nothing, frees nothing and keeps no pointer after a call returns.
+ *  - Layouts are dense row-major in the shapes given. "dtype" arrays hold fp32 (SSM_DTYPE_F32) or
+ *    bf16 (SSM_DTYPE_BF16) elements; A_log, states, h0 and final_state are always fp32.
+ *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy default
+ *    stream) and runs asynchronously; the return code covers argument checks and launch errors.
+ *    ssm_check_device() synchronises the stream and reports errors raised while kernels ran.
+ *  - N (state size) must be in [1, 16]; larger N returns SSM_ERR_UNSUPPORTED.
+ *  - Outputs may not overlap inputs (checked on the pointer ranges: SSM_ERR_INVALID_ARG).
+ *  - Any status other than SSM_OK leaves a one-line reason in ssm_last_error() (per thread).
+ *  - Results are deterministic for a given shape, dtype and device (no atomics on the data path).
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum, overlapping in/out ranges */
+    SSM_ERR_UNSUPPORTED = 2,  /* valid but not implemented (N > 16) */
+    SSM_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    SSM_ERR_TIMEOUT = 4       /* a kernel gave up a bounded wait (reported by ssm_check_device) */
+} ssm_status;
+
+typedef enum { SSM_DISC_EULER = 0, SSM_DISC_ZOH = 1 } ssm_disc;
+typedef enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 1 } ssm_dtype;
+
+/*
+ * Prefill scan over whole sequences ("Understanding Mamba" s7: discretisation, recurrence and readout
+ * fused so that the [batch, L, D, N] states never leave the chip).
+ *   x, delta    [batch, L, D]  dtype      input sequence and per-step step size
+ *   A_log       [D, N]         fp32       A = -exp(A_log)
+ *   B, C        [batch, L, N]  dtype      input / output projections, shared by all D channels
+ *   h0          [batch, D, N]  fp32       initial state, or NULL for zeros
+ *   y           [batch, L, D]  dtype      output (bf16 outputs are rounded to nearest even)
+ *   final_state [batch, D, N]  fp32       state after step L-1 (h0 or zeros when L == 0), or NULL
+ * batch, L, D >= 0 (zero sizes are no-ops apart from final_state). final_state may not overlap h0.
+ */
+ssm_status ssm_scan_fwd(const void *x, const void *delta, const float *A_log,
+                        const void *B, const void *C, const float *h0,
+                        void *y, float *final_state,
+                        int64_t batch, int64_t L, int64_t D, int64_t N,
+                        ssm_dtype dtype, ssm_disc disc, void *stream);
+
+/*
+ * One recurrent decode step ("Understanding Mamba" s3.2 and s10.1: the same Eq. (3) body applied
+ * once to a carried state; constant work per token).
+ *   state    [batch, D, N]  fp32   read and updated in place
+ *   x_t, delta_t [batch, D] dtype
+ *   A_log    [D, N]         fp32
+ *   B_t, C_t [batch, N]     dtype
+ *   y_t      [batch, D]     dtype  output
+ */
+ssm_status ssm_scan_step(float *state, const void *x_t, const void *delta_t, const float *A_log,
+                         const void *B_t, const void *C_t, void *y_t,
+                         int64_t batch, int64_t D, int64_t N,
+                         ssm_dtype dtype, ssm_disc disc, void *stream);
+
+/* Synchronise `stream` and report any error raised while this library's kernels ran on it. */
+ssm_status ssm_check_device(void *stream);
+
+/* Static name of a status code. */
+const char *ssm_status_string(ssm_status s);
+
+/* One-line reason for the last non-OK status returned on the calling thread ("" if none). */
+const char *ssm_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

@@ -1,0 +1,139 @@
+"""B300-native selective scan (Mamba): a C-ABI CUDA library for sm_103a and this thin binding.
+
+    y, final_state = ssm_scan_fwd(x, delta, A_log, B, C, disc="euler" | "zoh", h0=None)
+    y_t = ssm_scan_step(state, x_t, delta_t, A_log, B_t, C_t, disc=...)   # state updated in place
+
+Arguments are torch tensors: x, delta [batch, L, D] and B, C [batch, L, N] in float32 or bfloat16
+(all four the same), A_log [D, N] float32, states float32. CUDA tensors run on the caller's current
+stream. CPU tensors are copied to the current CUDA device (asynchronously when pinned), processed, and
+the results copied back. Every arithmetic step runs in the library's kernels; this module only
+marshals arguments (see include/ssm_scan.h for the contract).
+"""
+from __future__ import annotations
+
+from . import _ffi
+from ._ffi import SsmError
+
+__all__ = ["ssm_scan_fwd", "ssm_scan_step", "ssm_scan_fwd_ptr", "ssm_scan_step_ptr", "check_device",
+           "SsmError", "version"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return _ffi.DTYPE["f32"]
+    if t.dtype == torch.bfloat16:
+        return _ffi.DTYPE["bf16"]
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes_void(s.cuda_stream)
+
+
+def ctypes_void(v):
+    import ctypes
+    return ctypes.c_void_p(v) if v else None
+
+
+def _ptr(t):
+    return None if t is None else ctypes_void(t.data_ptr())
+
+
+def version() -> int:
+    return _ffi.load().ssm_version()
+
+
+def ssm_scan_fwd_ptr(x, delta, A_log, B, C, h0, y, final_state, batch, L, D, N, dtype, disc, stream):
+    """Raw C-ABI call on integer device addresses (0 for NULL); dtype "f32"/"bf16", disc "euler"/"zoh"."""
+    v = ctypes_void
+    st = _ffi.load().ssm_scan_fwd(v(x), v(delta), v(A_log), v(B), v(C), v(h0), v(y), v(final_state),
+                                  batch, L, D, N, _ffi.DTYPE[dtype], _ffi.DISC[disc], v(stream))
+    _ffi.check("ssm_scan_fwd", st)
+
+
+def ssm_scan_step_ptr(state, x_t, delta_t, A_log, B_t, C_t, y_t, batch, D, N, dtype, disc, stream):
+    """Raw C-ABI call on integer device addresses."""
+    v = ctypes_void
+    st = _ffi.load().ssm_scan_step(v(state), v(x_t), v(delta_t), v(A_log), v(B_t), v(C_t), v(y_t),
+                                   batch, D, N, _ffi.DTYPE[dtype], _ffi.DISC[disc], v(stream))
+    _ffi.check("ssm_scan_step", st)
+
+
+def _to_device(ts, device):
+    return [None if t is None else t.to(device, non_blocking=True) for t in ts]
+
+
+def ssm_scan_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, y=None, final_state=None,
+                 want_final_state: bool = True, stream=None):
+    """Prefill selective scan. Returns (y, final_state) (final_state None if not wanted)."""
+    torch = _torch()
+    if x.device.type == "cpu":
+        dev = torch.device("cuda", torch.cuda.current_device())
+        xd, dd, ad, bd, cd, hd = _to_device([x, delta, A_log, B, C, h0], dev)
+        yd, fd = ssm_scan_fwd(xd, dd, ad, bd, cd, disc, hd, want_final_state=want_final_state, stream=stream)
+        torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+        return yd.cpu(), None if fd is None else fd.cpu()
+    batch, L, D = x.shape
+    N = A_log.shape[-1]
+    code = _dtype_code(x)
+    for name, t in (("delta", delta), ("B", B), ("C", C)):
+        if t.dtype != x.dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, x has {x.dtype}")
+    if A_log.dtype != torch.float32 or (h0 is not None and h0.dtype != torch.float32):
+        raise TypeError("A_log and h0 must be float32")
+    if tuple(delta.shape) != (batch, L, D) or tuple(B.shape) != (batch, L, N) or tuple(C.shape) != (batch, L, N) \
+            or tuple(A_log.shape) != (D, N) or (h0 is not None and tuple(h0.shape) != (batch, D, N)):
+        raise ValueError("shape mismatch: x/delta [b,L,D], B/C [b,L,N], A_log [D,N], h0 [b,D,N]")
+    ts = [x, delta, A_log, B, C] + ([h0] if h0 is not None else [])
+    if any(not t.is_contiguous() for t in ts) or any(t.device != x.device for t in ts):
+        raise ValueError("inputs must be contiguous and on one device")
+    if y is None:
+        y = torch.empty((batch, L, D), dtype=x.dtype, device=x.device)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((batch, D, N), dtype=torch.float32, device=x.device)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    st = _ffi.load().ssm_scan_fwd(_ptr(x), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(h0), _ptr(y),
+                                  _ptr(final_state), batch, L, D, N, code, _ffi.DISC[disc],
+                                  ctypes_void(s.cuda_stream))
+    _ffi.check("ssm_scan_fwd", st)
+    return y, final_state
+
+
+def ssm_scan_step(state, x_t, delta_t, A_log, B_t, C_t, disc: str = "euler", *, y_t=None, stream=None):
+    """One decode step: updates ``state`` [batch, D, N] in place and returns y_t [batch, D]."""
+    torch = _torch()
+    batch, D, N = state.shape
+    code = _dtype_code(x_t)
+    if state.dtype != torch.float32 or A_log.dtype != torch.float32:
+        raise TypeError("state and A_log must be float32")
+    for name, t in (("delta_t", delta_t), ("B_t", B_t), ("C_t", C_t)):
+        if t.dtype != x_t.dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, x_t has {x_t.dtype}")
+    if tuple(x_t.shape) != (batch, D) or tuple(delta_t.shape) != (batch, D) or tuple(B_t.shape) != (batch, N) \
+            or tuple(C_t.shape) != (batch, N) or tuple(A_log.shape) != (D, N):
+        raise ValueError("shape mismatch: state [b,D,N], x_t/delta_t [b,D], B_t/C_t [b,N], A_log [D,N]")
+    ts = [state, x_t, delta_t, A_log, B_t, C_t]
+    if any(not t.is_contiguous() for t in ts) or any(t.device != state.device for t in ts):
+        raise ValueError("inputs must be contiguous and on one device")
+    if y_t is None:
+        y_t = torch.empty((batch, D), dtype=x_t.dtype, device=state.device)
+    s = stream if stream is not None else torch.cuda.current_stream(state.device)
+    st = _ffi.load().ssm_scan_step(_ptr(state), _ptr(x_t), _ptr(delta_t), _ptr(A_log), _ptr(B_t), _ptr(C_t),
+                                   _ptr(y_t), batch, D, N, code, _ffi.DISC[disc], ctypes_void(s.cuda_stream))
+    _ffi.check("ssm_scan_step", st)
+    return y_t
+
+
+def check_device(stream=None) -> None:
+    """Synchronise the stream and raise SsmError if a kernel of this library failed on it."""
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _ffi.check("ssm_check_device", _ffi.load().ssm_check_device(ctypes_void(s.cuda_stream)))

@@ -1,0 +1,147 @@
+// api.cu -- the C ABI declared in include/ssm_scan.h: argument checks, kernel choice, launch, status.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/ssm_scan.h"
+#include "launch.h"
+
+namespace ssm {
+
+namespace {
+thread_local char g_last_error[256] = "";
+
+ssm_status fail(ssm_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+ssm_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(SSM_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+struct Range {
+  uintptr_t lo, hi;
+};
+Range range_of(const void* p, int64_t count, int64_t elem) {
+  uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + static_cast<uintptr_t>(count) * static_cast<uintptr_t>(elem)};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+bool valid_enums(ssm_dtype dt, ssm_disc disc) {
+  return (dt == SSM_DTYPE_F32 || dt == SSM_DTYPE_BF16) && (disc == SSM_DISC_EULER || disc == SSM_DISC_ZOH);
+}
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > INT64_MAX / a) return false;
+  *out = a * b;
+  return true;
+}
+}  // namespace
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
+}  // namespace ssm
+
+using namespace ssm;
+
+extern "C" {
+
+ssm_status ssm_scan_fwd(const void* x, const void* delta, const float* A_log, const void* B, const void* C,
+                        const float* h0, void* y, float* final_state, int64_t batch, int64_t L, int64_t D,
+                        int64_t N, ssm_dtype dtype, ssm_disc disc, void* stream) {
+  g_last_error[0] = '\0';
+  if (!valid_enums(dtype, disc)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: bad dtype or disc");
+  if (batch < 0 || L < 0 || D < 0 || N < 1)
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: sizes must be >= 0 and N >= 1");
+  if (N > 16) return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd: N = %lld > 16", (long long)N);
+  int64_t bl, bld, bln, bd, bdn;
+  if (!mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bl, N, &bln) || !mul_ok(batch, D, &bd) ||
+      !mul_ok(bd, N, &bdn))
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: sizes overflow");
+  const int64_t es = dtype == SSM_DTYPE_BF16 ? 2 : 4;
+  if (bld > 0 && (!x || !delta || !y)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: null x/delta/y");
+  if (bln > 0 && (!B || !C)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: null B/C");
+  if (bld > 0 && !A_log) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: null A_log");
+  const Range ry = range_of(y, bld, es);
+  const Range rf = range_of(final_state, final_state ? bdn : 0, 4);
+  const Range ins[] = {range_of(x, bld, es), range_of(delta, bld, es), range_of(A_log, D * N, 4),
+                       range_of(B, bln, es), range_of(C, bln, es), range_of(h0, h0 ? bdn : 0, 4)};
+  for (const Range& r : ins)
+    if (overlap(ry, r) || overlap(rf, r)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: outputs overlap inputs");
+  if (overlap(ry, rf)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: y overlaps final_state");
+
+  FwdArgs a{x, delta, A_log, B, C, h0, y, final_state, batch, L, D, N, static_cast<int>(dtype),
+            static_cast<int>(disc), static_cast<cudaStream_t>(stream)};
+  if (batch == 0 || D == 0) return SSM_OK;
+  cudaError_t e = (L == 0) ? launch_init_state(a) : launch_fwd_simple(a);
+  if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd launch");
+  return SSM_OK;
+}
+
+ssm_status ssm_scan_step(float* state, const void* x_t, const void* delta_t, const float* A_log,
+                         const void* B_t, const void* C_t, void* y_t, int64_t batch, int64_t D, int64_t N,
+                         ssm_dtype dtype, ssm_disc disc, void* stream) {
+  g_last_error[0] = '\0';
+  if (!valid_enums(dtype, disc)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_step: bad dtype or disc");
+  if (batch < 0 || D < 0 || N < 1)
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_step: sizes must be >= 0 and N >= 1");
+  if (N > 16) return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_step: N = %lld > 16", (long long)N);
+  int64_t bd, bdn, bn;
+  if (!mul_ok(batch, D, &bd) || !mul_ok(bd, N, &bdn) || !mul_ok(batch, N, &bn))
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_step: sizes overflow");
+  if (bd == 0) return SSM_OK;
+  if (!state || !x_t || !delta_t || !A_log || !B_t || !C_t || !y_t)
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_step: null pointer");
+  const int64_t es = dtype == SSM_DTYPE_BF16 ? 2 : 4;
+  const Range rs = range_of(state, bdn, 4), ry = range_of(y_t, bd, es);
+  const Range ins[] = {range_of(x_t, bd, es), range_of(delta_t, bd, es), range_of(A_log, D * N, 4),
+                       range_of(B_t, bn, es), range_of(C_t, bn, es)};
+  for (const Range& r : ins)
+    if (overlap(rs, r) || overlap(ry, r)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_step: outputs overlap inputs");
+  if (overlap(rs, ry)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_step: y_t overlaps state");
+  StepArgs a{state, x_t, delta_t, A_log, B_t, C_t, y_t, batch, D, N, static_cast<int>(dtype),
+             static_cast<int>(disc), static_cast<cudaStream_t>(stream)};
+  cudaError_t e = launch_step(a);
+  if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_step launch");
+  return SSM_OK;
+}
+
+ssm_status ssm_check_device(void* stream) {
+  g_last_error[0] = '\0';
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ssm_check_device");
+  return SSM_OK;
+}
+
+const char* ssm_status_string(ssm_status s) {
+  switch (s) {
+    case SSM_OK: return "SSM_OK";
+    case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
+    case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT";
+  }
+  return "SSM_ERR_UNKNOWN";
+}
+
+const char* ssm_last_error(void) { return g_last_error; }
+
+int ssm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// launch.h -- host-side launchers shared between the C ABI (api.cu) and the kernel files.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ssm {
+
+struct FwdArgs {
+  const void* x;
+  const void* delta;
+  const float* A_log;
+  const void* B;
+  const void* C;
+  const float* h0;
+  void* y;
+  float* final_state;
+  int64_t batch, L, D, N;
+  int dtype;  // 0 f32, 1 bf16
+  int disc;   // 0 euler, 1 zoh
+  cudaStream_t stream;
+};
+
+struct StepArgs {
+  float* state;
+  const void* x;
+  const void* delta;
+  const float* A_log;
+  const void* B;
+  const void* C;
+  void* y;
+  int64_t batch, D, N;
+  int dtype;
+  int disc;
+  cudaStream_t stream;
+};
+
+int sm_count();  // multiprocessors of the current device (cached per device)
+
+cudaError_t launch_fwd_simple(const FwdArgs& a);
+cudaError_t launch_init_state(const FwdArgs& a);  // final_state = h0 or 0 (used when L == 0)
+cudaError_t launch_step(const StepArgs& a);
+
+}  // namespace ssm

@@ -1,0 +1,216 @@
+// scan_fwd_simple.cu -- general-shape prefill scan (any D, any N in [1, 16], any alignment).
+//
+// Work layout: one lane per channel d, one warp per 32 consecutive channels of one batch element
+// (a "row"). The rows' time axes are laid end to end and cut into equal contiguous pieces, one per warp
+// of the grid, so every warp gets the same number of (row, t) steps whatever the shape.
+//
+// A piece that starts at t0 > 0 first rebuilds the state entering t0 with no communication: it walks the
+// preceding steps backwards and accumulates
+//     h(t0-1) = sum_j ( prod_{k=j+1..t0-1} Abar_k ) * Bbar_j x_j          ("Mathematical Prerequisites for
+//                                                                          Mamba" s6, unrolled sum)
+// stopping once every decay product is below kCarryEps (the rest is at most that fraction of the state
+// there) or at t = 0, where the sum is exact (plus prod * h0 when an initial state is given). It then
+// runs the recurrence of "Understanding Mamba" Eq. (3) forward over its own steps, writing y.
+//
+// Discretisation: Abar = exp(delta A) (SFU exp2), Euler Bbar = delta B, ZOH Bbar = (e^{delta A}-1)/A B with
+// e^z - 1 taken from a Taylor polynomial for small |z| (no cancellation), delta B where A == 0.
+#include "common.cuh"
+#include "launch.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kWarps = 4;           // warps per CTA
+constexpr int kMinPiece = 128;      // shortest piece worth a separate warp
+
+struct SimpleParams {
+  const void* x;
+  const void* delta;
+  const float* A_log;
+  const void* B;
+  const void* C;
+  const float* h0;
+  void* y;
+  float* final_state;
+  int64_t batch, L, D, N;
+  int64_t groups;   // ceil(D / 32)
+  int64_t total;    // batch * groups * L
+  int64_t nwarps;   // warps taking part
+};
+
+template <int NP, bool ZOH>
+struct Chan {
+  float A[NP];     // A = -exp(A_log)
+  float A2[NP];    // A * log2(e)
+  float invA[NP];  // 1 / A (ZOH), 0 where A == 0
+  bool zeroA[NP];
+};
+
+template <int NP, bool ZOH, typename T>
+__device__ __forceinline__ void bbar_x(const Chan<NP, ZOH>& c, int n, float dt, float x, float b, float a,
+                                      float& bx) {
+  if (ZOH) {
+    float e = expm1_small(dt * c.A[n], a);  // e^{delta A} - 1
+    float coef = c.zeroA[n] ? dt : e * c.invA[n];
+    bx = coef * b * x;
+  } else {
+    bx = dt * b * x;
+  }
+}
+
+template <int NP, bool ZOH, typename T>
+__global__ void __launch_bounds__(kWarps * 32) scan_fwd_simple_kernel(SimpleParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  if (gw >= p.nwarps) return;  // whole warp leaves together
+  int64_t lo = static_cast<int64_t>(static_cast<__int128>(gw) * p.total / p.nwarps);
+  const int64_t hi = static_cast<int64_t>(static_cast<__int128>(gw + 1) * p.total / p.nwarps);
+  const int N = static_cast<int>(p.N);
+  while (lo < hi) {
+    const int64_t row = lo / p.L;
+    const int64_t t0 = lo % p.L;
+    const int64_t t1 = (hi - lo < p.L - t0) ? t0 + (hi - lo) : p.L;
+    lo += t1 - t0;
+    const int64_t b = row / p.groups;
+    const int64_t d = (row % p.groups) * 32 + lane;
+    const bool act = d < p.D;
+
+    Chan<NP, ZOH> c;
+#pragma unroll
+    for (int n = 0; n < NP; ++n) {
+      float A = -1.0f;
+      if (act && n < N) A = -expf(__ldg(p.A_log + d * N + n));
+      c.A[n] = A;
+      c.A2[n] = A * kLog2e;
+      c.zeroA[n] = (A == 0.0f);
+      c.invA[n] = c.zeroA[n] ? 0.0f : 1.0f / A;
+    }
+    const float* h0row = p.h0 ? p.h0 + (b * p.D + d) * N : nullptr;
+
+    // ---- state entering t0 -------------------------------------------------------------------
+    float h[NP];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) h[n] = 0.0f;
+    if (t0 == 0) {
+      if (h0row && act) {
+#pragma unroll
+        for (int n = 0; n < NP; ++n)
+          if (n < N) h[n] = h0row[n];
+      }
+    } else {
+      float P[NP];
+#pragma unroll
+      for (int n = 0; n < NP; ++n) P[n] = 1.0f;
+      int64_t j = t0 - 1;
+      int64_t steps = 0;
+      while (true) {
+        const int64_t xi = (b * p.L + j) * p.D + d;
+        const float xv = act ? Elem<T>::load(p.x, xi) : 0.0f;
+        const float dt = act ? Elem<T>::load(p.delta, xi) : 0.0f;
+        const int64_t bi = (b * p.L + j) * N;
+#pragma unroll
+        for (int n = 0; n < NP; ++n) {
+          const float bn = (n < N) ? Elem<T>::load(p.B, bi + n) : 0.0f;
+          const float z = dt * c.A2[n];
+          const float a = ex2(z);
+          float bx;
+          bbar_x<NP, ZOH, T>(c, n, dt, xv, bn, a, bx);
+          h[n] = fmaf(P[n], bx, h[n]);
+          P[n] *= a;
+        }
+        ++steps;
+        if (j == 0) {
+          if (h0row && act) {
+#pragma unroll
+            for (int n = 0; n < NP; ++n)
+              if (n < N) h[n] = fmaf(P[n], h0row[n], h[n]);
+          }
+          break;
+        }
+        --j;
+        if ((steps & 7) == 0) {
+          float pm = 0.0f;
+#pragma unroll
+          for (int n = 0; n < NP; ++n) pm = fmaxf(pm, fabsf(P[n]));
+          if (!act) pm = 0.0f;
+          if (!__any_sync(0xffffffffu, pm >= kCarryEps)) break;
+        }
+      }
+    }
+
+    // ---- forward over [t0, t1) -------------------------------------------------------------------
+    for (int64_t t = t0; t < t1; ++t) {
+      const int64_t xi = (b * p.L + t) * p.D + d;
+      const float xv = act ? Elem<T>::load(p.x, xi) : 0.0f;
+      const float dt = act ? Elem<T>::load(p.delta, xi) : 0.0f;
+      const int64_t bi = (b * p.L + t) * N;
+      float yv = 0.0f;
+#pragma unroll
+      for (int n = 0; n < NP; ++n) {
+        const float bn = (n < N) ? Elem<T>::load(p.B, bi + n) : 0.0f;
+        const float cn = (n < N) ? Elem<T>::load(p.C, bi + n) : 0.0f;
+        const float z = dt * c.A2[n];
+        const float a = ex2(z);
+        float bx;
+        bbar_x<NP, ZOH, T>(c, n, dt, xv, bn, a, bx);
+        h[n] = fmaf(a, h[n], bx);
+        yv = fmaf(cn, h[n], yv);
+      }
+      if (act) Elem<T>::store(p.y, xi, yv);
+    }
+    if (t1 == p.L && p.final_state && act) {
+      float* fs = p.final_state + (b * p.D + d) * N;
+#pragma unroll
+      for (int n = 0; n < NP; ++n)
+        if (n < N) fs[n] = h[n];
+    }
+  }
+}
+
+template <int NP, bool ZOH, typename T>
+cudaError_t launch_np(const SimpleParams& sp, cudaStream_t s) {
+  const int64_t blocks = (sp.nwarps + kWarps - 1) / kWarps;
+  scan_fwd_simple_kernel<NP, ZOH, T><<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(sp);
+  return cudaGetLastError();
+}
+
+template <bool ZOH, typename T>
+cudaError_t launch_disc(const SimpleParams& sp, cudaStream_t s) {
+  if (sp.N <= 4) return launch_np<4, ZOH, T>(sp, s);
+  if (sp.N <= 8) return launch_np<8, ZOH, T>(sp, s);
+  return launch_np<16, ZOH, T>(sp, s);
+}
+
+__global__ void init_state_kernel(const float* h0, float* out, int64_t n) {
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = h0 ? h0[i] : 0.0f;
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simple(const FwdArgs& a) {
+  SimpleParams sp;
+  sp.x = a.x; sp.delta = a.delta; sp.A_log = a.A_log; sp.B = a.B; sp.C = a.C; sp.h0 = a.h0;
+  sp.y = a.y; sp.final_state = a.final_state;
+  sp.batch = a.batch; sp.L = a.L; sp.D = a.D; sp.N = a.N;
+  sp.groups = (a.D + 31) / 32;
+  const int64_t rows = a.batch * sp.groups;
+  sp.total = rows * a.L;
+  const int64_t want = static_cast<int64_t>(sm_count()) * 16;  // 4 CTAs x 4 warps per SM
+  int64_t nw = rows * ((a.L + kMinPiece - 1) / kMinPiece);
+  if (nw > want) nw = want;
+  if (nw < 1) nw = 1;
+  sp.nwarps = nw;
+  if (a.disc == 1)
+    return a.dtype == 1 ? launch_disc<true, __nv_bfloat16>(sp, a.stream) : launch_disc<true, float>(sp, a.stream);
+  return a.dtype == 1 ? launch_disc<false, __nv_bfloat16>(sp, a.stream) : launch_disc<false, float>(sp, a.stream);
+}
+
+cudaError_t launch_init_state(const FwdArgs& a) {
+  const int64_t n = a.batch * a.D * a.N;
+  if (n == 0 || a.final_state == nullptr) return cudaSuccess;
+  init_state_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, a.stream>>>(a.h0, a.final_state, n);
+  return cudaGetLastError();
+}
+
+}  // namespace ssm

@@ -71,7 +71,7 @@ def _normal(rng, shape, mu=0.0, sigma=1.0) -> np.ndarray:
 def a_log_s4d(D: int, N: int) -> np.ndarray:
     """A_log[d, n] = log(n + 1) (float32), i.e. A[d, n] = -(n + 1) for every channel."""
     row = np.array([math.log(n + 1) for n in range(N)], dtype=np.float32)
-    return np.ascontiguousarray(np.broadcast_to(row, (D, N)))
+    return np.tile(row, (D, 1))
 
 
 def make_inputs(batch, L, D, N, seed=0, mu=-2.0, sigma=1.0, dtype="f32", a_log=None, **_):

@@ -1,0 +1,86 @@
+"""The C-ABI library loads, exports every symbol include/ssm_scan.h declares, and rejects bad
+arguments before touching the GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_124_b300 import _ffi, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ssm_scan.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _ffi.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = declared_symbols()
+    assert "ssm_scan_fwd" in syms and "ssm_scan_step" in syms
+    for s in syms:
+        assert hasattr(lib, s), f"{s} declared in ssm_scan.h but not exported"
+        assert s in _ffi.SIGNATURES, f"{s} has no ctypes signature in the binding"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.ssm_version() >= 100
+    for code, name in enumerate(["SSM_OK", "SSM_ERR_INVALID_ARG", "SSM_ERR_UNSUPPORTED", "SSM_ERR_CUDA",
+                                 "SSM_ERR_TIMEOUT"]):
+        assert lib.ssm_status_string(code).decode() == name
+
+
+FAKE = 1 << 40  # never dereferenced: every case below fails validation first
+
+
+def fwd(lib, *, x=FAKE, delta=FAKE + (1 << 30), A_log=FAKE + (2 << 30), B=FAKE + (3 << 30), C=FAKE + (4 << 30),
+        h0=None, y=FAKE + (5 << 30), fs=FAKE + (6 << 30), batch=1, L=8, D=4, N=16, dtype=0, disc=0):
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+    return lib.ssm_scan_fwd(v(x), v(delta), v(A_log), v(B), v(C), v(h0), v(y), v(fs), batch, L, D, N, dtype,
+                            disc, None)
+
+
+def test_fwd_argument_errors(lib):
+    assert fwd(lib, N=17) == _ffi.SSM_ERR_UNSUPPORTED
+    assert b"N = 17" in lib.ssm_last_error()
+    assert fwd(lib, N=0) == _ffi.SSM_ERR_INVALID_ARG
+    assert fwd(lib, L=-1) == _ffi.SSM_ERR_INVALID_ARG
+    assert fwd(lib, dtype=7) == _ffi.SSM_ERR_INVALID_ARG
+    assert fwd(lib, disc=2) == _ffi.SSM_ERR_INVALID_ARG
+    assert fwd(lib, x=None) == _ffi.SSM_ERR_INVALID_ARG
+    assert fwd(lib, B=None) == _ffi.SSM_ERR_INVALID_ARG
+    assert fwd(lib, A_log=None) == _ffi.SSM_ERR_INVALID_ARG
+    assert fwd(lib, y=FAKE + 16) == _ffi.SSM_ERR_INVALID_ARG            # y overlaps x
+    assert b"overlap" in lib.ssm_last_error()
+    assert fwd(lib, h0=FAKE + (7 << 30), fs=FAKE + (7 << 30) + 8) == _ffi.SSM_ERR_INVALID_ARG  # final overlaps h0
+    assert fwd(lib, batch=1 << 40, L=1 << 20, D=1 << 20) == _ffi.SSM_ERR_INVALID_ARG  # size overflow
+    assert fwd(lib, batch=0) == _ffi.SSM_OK                            # nothing to do, no GPU touched
+    assert fwd(lib, D=0, x=None, y=None) == _ffi.SSM_OK
+
+
+def test_step_argument_errors(lib):
+    v = ctypes.c_void_p
+    args = [v(FAKE), v(FAKE + (1 << 30)), v(FAKE + (2 << 30)), v(FAKE + (3 << 30)), v(FAKE + (4 << 30)),
+            v(FAKE + (5 << 30)), v(FAKE + (6 << 30))]
+    assert lib.ssm_scan_step(*args, 2, 8, 17, 0, 0, None) == _ffi.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_scan_step(*args, 2, 8, 16, 3, 0, None) == _ffi.SSM_ERR_INVALID_ARG
+    bad = list(args)
+    bad[6] = v(FAKE + 4)  # y_t overlaps state
+    assert lib.ssm_scan_step(*bad, 2, 8, 16, 0, 0, None) == _ffi.SSM_ERR_INVALID_ARG
+    bad = list(args)
+    bad[1] = None
+    assert lib.ssm_scan_step(*bad, 2, 8, 16, 0, 0, None) == _ffi.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_step(*args, 0, 8, 16, 0, 0, None) == _ffi.SSM_OK
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        _ffi.load(str(tmp_path / "libssm_scan.so"))

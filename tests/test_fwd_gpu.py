@@ -1,0 +1,200 @@
+"""Parity of the CUDA prefill scan (ssm_scan_fwd, through the C ABI) with the fp64 oracle."""
+import numpy as np
+import pytest
+
+import ssm_inputs
+from gpu_util import host_values, run_fwd
+from tolerance import TOL, rel_err, rel_err_elementwise
+
+pytestmark = pytest.mark.gpu
+
+
+def check_fwd(orc, inp, dtype, disc, h0=None, channels=None):
+    y, fs = run_fwd(inp, dtype, disc, h0=h0)
+    hv = host_values(inp, dtype)
+    batch, L, D = hv["x"].shape
+    if channels is None:
+        yr, sr = orc.scan_fwd(hv["x"], hv["delta"], inp["A_log"], hv["B"], hv["C"], disc=disc, h0=h0)
+        ey, es = rel_err(y, yr), rel_err(fs, sr)
+    else:
+        h0c = None if h0 is None else h0.reshape(batch * D, -1)[channels]
+        yr, sr = orc.scan_fwd(hv["x"], hv["delta"], inp["A_log"], hv["B"], hv["C"], disc=disc, h0=h0c,
+                              channels=channels)
+        b, d = np.divmod(np.asarray(channels), D)
+        yg = y[b, :, d]
+        sg = fs[b, d]
+        ey, es = rel_err(yg, yr), rel_err(sg, sr)
+    tol = TOL[dtype]
+    assert ey <= tol, f"y rel err {ey:.3g} > {tol}"
+    assert es <= tol, f"final state rel err {es:.3g} > {tol}"
+    return ey, es
+
+
+SHAPES = [
+    # batch, L, D, N  -- spans several warps, pieces with a backward carry, ragged channel tails
+    (1, 1, 1, 1),
+    (1, 7, 3, 3),
+    (2, 300, 70, 16),
+    (3, 1000, 33, 5),
+    (1, 4096, 64, 16),
+    (2, 777, 130, 8),
+    (1, 20000, 32, 16),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"b{s[0]}_L{s[1]}_D{s[2]}_N{s[3]}" for s in SHAPES])
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fwd_shapes(orc, shape, disc, dtype):
+    batch, L, D, N = shape
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=L + D, mu=-2.0, sigma=1.0, dtype=dtype)
+    check_fwd(orc, inp, dtype, disc)
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_fwd_initial_state(orc, disc):
+    batch, L, D, N = 2, 3000, 40, 16
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=1)
+    h0 = np.random.default_rng(2).standard_normal((batch, D, N)).astype(np.float32)
+    check_fwd(orc, inp, "f32", disc, h0=h0)
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_fwd_long_memory(orc, disc):
+    """Small delta: the carry into each piece reaches far back (down to t = 0 for some pieces)."""
+    inp = ssm_inputs.make_inputs(1, 8192, 64, 16, seed=3, mu=-9.0, sigma=1.0)
+    check_fwd(orc, inp, "f32", disc)
+
+
+def test_fwd_negative_delta(orc):
+    """delta < 0 makes Abar > 1: nothing decays, every piece reconstructs its state from t = 0."""
+    inp = ssm_inputs.make_inputs(1, 4096, 32, 4, seed=4)
+    inp["delta"] = (np.random.default_rng(5).uniform(-1e-3, 1e-3, inp["delta"].shape)).astype(np.float32)
+    check_fwd(orc, inp, "f32", "euler")
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_fwd_degenerate_A(orc, disc):
+    """A_log very negative: A underflows to 0 in float32 (ZOH takes its A -> 0 limit delta*B), or is tiny."""
+    batch, L, D, N = 1, 600, 40, 8
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=6)
+    A_log = ssm_inputs.a_log_s4d(D, N).copy()
+    A_log[:, 0] = -200.0
+    A_log[:, 1] = -60.0
+    A_log[::3, 2] = 5.0
+    inp["A_log"] = A_log
+    check_fwd(orc, inp, "f32", disc)
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_fwd_delta_limits(orc, disc):
+    """delta -> 0 keeps the initial state; a huge delta resets it (ZOH: to -B x / A)."""
+    batch, L, D, N = 1, 500, 48, 16
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=8)
+    h0 = np.random.default_rng(9).standard_normal((batch, D, N)).astype(np.float32)
+    inp["delta"] = np.full_like(inp["delta"], 1e-30)
+    check_fwd(orc, inp, "f32", disc, h0=h0)
+    inp["delta"] = np.full_like(inp["delta"], 1e4)
+    check_fwd(orc, inp, "f32", disc, h0=h0)
+
+
+def test_fwd_zero_length_and_empty():
+    import torch
+    import selective_state_space_124_b300 as lib
+    x = torch.zeros((2, 0, 8), device="cuda")
+    B = torch.zeros((2, 0, 4), device="cuda")
+    A_log = torch.zeros((8, 4), device="cuda")
+    h0 = torch.randn((2, 8, 4), device="cuda")
+    y, fs = lib.ssm_scan_fwd(x, x, A_log, B, B, h0=h0)
+    assert y.shape == (2, 0, 8)
+    assert torch.equal(fs, h0)
+    _, fs = lib.ssm_scan_fwd(x, x, A_log, B, B)
+    assert torch.count_nonzero(fs) == 0
+    x = torch.zeros((0, 5, 8), device="cuda")
+    y, fs = lib.ssm_scan_fwd(x, x, A_log, torch.zeros((0, 5, 4), device="cuda"), torch.zeros((0, 5, 4), device="cuda"))
+    assert y.numel() == 0 and fs.numel() == 0
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_fwd_split_invariance(orc, disc):
+    """fwd over [0, L) == fwd over [0, k) then fwd from its final state over [k, L) (on the device)."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    from gpu_util import dev_inputs
+    batch, L, D, N, k = 2, 5000, 96, 16, 2222
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=10)
+    d = dev_inputs(inp, "f32")
+    y, fs = lib.ssm_scan_fwd(d["x"], d["delta"], d["A_log"], d["B"], d["C"], disc=disc)
+    sl = lambda t, a, b_: t[:, a:b_].contiguous()
+    y1, f1 = lib.ssm_scan_fwd(sl(d["x"], 0, k), sl(d["delta"], 0, k), d["A_log"], sl(d["B"], 0, k),
+                              sl(d["C"], 0, k), disc=disc)
+    y2, f2 = lib.ssm_scan_fwd(sl(d["x"], k, L), sl(d["delta"], k, L), d["A_log"], sl(d["B"], k, L),
+                              sl(d["C"], k, L), disc=disc, h0=f1)
+    assert rel_err(torch.cat([y1, y2], 1).cpu().numpy(), y.cpu().numpy()) <= 1e-5
+    assert rel_err(f2.cpu().numpy(), fs.cpu().numpy()) <= 1e-5
+
+
+def test_pins_through_gpu(orc):
+    """Page examples through the CUDA path (fp32 inputs): leaky bucket closed form, the 16-digit Euler
+    trace, the selective ZOH example."""
+    import math
+    from golden_io import load
+    # leaky bucket, ZOH, A = -1, B = C = 1, x = 1, delta = 1: y_t = 1 - e^{-(t+1)}
+    L = 64
+    inp = dict(x=np.ones((1, L, 1), np.float32), delta=np.ones((1, L, 1), np.float32),
+               B=np.ones((1, L, 1), np.float32), C=np.ones((1, L, 1), np.float32), A_log=np.zeros((1, 1), np.float32))
+    y, fs = run_fwd(inp, "f32", "zoh")
+    exact = 1.0 - np.exp(-np.arange(1, L + 1))
+    assert np.max(np.abs(y[0, :, 0] - exact)) < 1e-6
+    # 16-digit Euler trace
+    g = load("euler_scalar_trace.txt")
+    xs = np.asarray(g["x"], np.float32)
+    dts = np.asarray([math.log1p(math.exp(v - 5.0)) for v in g["x"]], np.float32)
+    inp = dict(x=xs.reshape(1, 4, 1), delta=dts.reshape(1, 4, 1), B=np.ones((1, 4, 1), np.float32),
+               C=np.ones((1, 4, 1), np.float32), A_log=np.zeros((1, 1), np.float32))
+    y, _ = run_fwd(inp, "f32", "euler")
+    assert np.max(np.abs(y[0, :, 0] - np.asarray(g["h"])) / np.asarray(g["h"])) < 2e-6
+    # selective ZOH example, N = 2
+    s = load("selective_zoh_n2.txt")
+    xv = np.asarray(s["x"])
+    dts = np.log1p(np.exp(2 * xv))
+    bc = (0.4 * xv[:, None] * np.ones((1, 2))).astype(np.float32).reshape(1, 4, 2)
+    inp = dict(x=xv.astype(np.float32).reshape(1, 4, 1), delta=dts.astype(np.float32).reshape(1, 4, 1),
+               B=bc, C=bc, A_log=np.log(-np.asarray(s["A"])).astype(np.float32).reshape(1, 2))
+    y, fs = run_fwd(inp, "f32", "zoh")
+    assert np.max(np.abs(y[0, :, 0] - np.asarray(s["y"]))) <= 5e-4 + 1e-6
+    assert np.max(np.abs(fs[0, 0] - np.asarray(s["h4"]))) <= 5e-4 + 1e-6
+
+
+# ---- the workloads at their full sizes, in the launch configuration the benchmark times -------------
+
+def test_workload_tiny(orc):
+    inp = ssm_inputs.workload_inputs("tiny")
+    check_fwd(orc, inp, "f32", "euler")
+
+
+@pytest.mark.slow
+def test_workload_mamba130m(orc):
+    inp = ssm_inputs.workload_inputs("mamba130m")
+    check_fwd(orc, inp, "f32", "euler")
+
+
+def _sample_channels(batch, D, k, seed):
+    rng = np.random.default_rng(seed)
+    ch = set(rng.choice(batch * D, size=min(k, batch * D), replace=False).tolist())
+    ch |= {0, D - 1, batch * D - 1, (batch - 1) * D, 31, 32}
+    return sorted(c for c in ch if c < batch * D)
+
+
+@pytest.mark.slow
+def test_workload_mamba1p4b_bf16(orc):
+    inp = ssm_inputs.workload_inputs("mamba1p4b")
+    cfg = inp["cfg"]
+    check_fwd(orc, inp, "bf16", "euler", channels=_sample_channels(cfg["batch"], cfg["D"], 192, 1))
+
+
+@pytest.mark.slow
+def test_workload_long_zoh(orc):
+    inp = ssm_inputs.workload_inputs("long")
+    cfg = inp["cfg"]
+    check_fwd(orc, inp, "f32", "zoh", channels=_sample_channels(cfg["batch"], cfg["D"], 96, 2))
