@@ -89,7 +89,7 @@ ssm_status ssm_scan_fwd(const void* x, const void* delta, const float* A_log, co
   FwdArgs a{x, delta, A_log, B, C, h0, y, final_state, batch, L, D, N, static_cast<int>(dtype),
             static_cast<int>(disc), static_cast<cudaStream_t>(stream)};
   if (batch == 0 || D == 0) return SSM_OK;
-  cudaError_t e = (L == 0) ? launch_init_state(a) : launch_fwd_simple(a);
+  cudaError_t e = (L == 0) ? launch_init_state(a) : (tma_path_ok(a) ? launch_fwd_tma(a) : launch_fwd_simple(a));
   if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd launch");
   return SSM_OK;
 }
@@ -126,6 +126,9 @@ ssm_status ssm_check_device(void* stream) {
   g_last_error[0] = '\0';
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "ssm_check_device");
+  const int st = read_and_clear_device_status();
+  if (st < 0) return fail(SSM_ERR_CUDA, "ssm_check_device: cannot read the device status word");
+  if (st != 0) return fail(SSM_ERR_TIMEOUT, "ssm_check_device: a kernel gave up a bounded wait");
   return SSM_OK;
 }
 

@@ -19,16 +19,16 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// e^z - 1 without cancellation for small |z|: a Taylor polynomial of degree 6 for |z| < 1/8 (remainder
-// below 1e-10 relative there), else expz - 1 where expz is an approximation of e^z.
-__device__ __forceinline__ float expm1_small(float z, float expz) {
-  float p = fmaf(z, 1.0f / 720.0f, 1.0f / 120.0f);
-  p = fmaf(z, p, 1.0f / 24.0f);
-  p = fmaf(z, p, 1.0f / 6.0f);
-  p = fmaf(z, p, 0.5f);
-  p = fmaf(z, p, 1.0f);
-  p *= z;
-  return fabsf(z) < 0.125f ? p : expz - 1.0f;
+// 2^w - 1 with no cancellation for small |w| (w = delta * A * log2(e)): Taylor series in w (coefficients
+// ln2^k / k!) for |w ln 2| < 1/32 (remainder below 1e-8 relative), else a - 1 with a the SFU value of
+// 2^w. Applying a decay as h + (2^w - 1) h keeps the factor exact to one rounding even when nothing decays
+// for many steps (the SFU value's tiny bias near 1 would otherwise accumulate).
+__device__ __forceinline__ float exp2m1(float w, float a) {
+  float q = fmaf(w, 0.009618129107628477f, 0.05550410866482158f);
+  q = fmaf(w, q, 0.2402265069591007f);
+  q = fmaf(w, q, 0.6931471805599453f);
+  q *= w;
+  return fabsf(w) < 0.04508422002825452f ? q : a - 1.0f;
 }
 
 template <typename T> struct Elem;

@@ -37,6 +37,9 @@ struct StepArgs {
 int sm_count();  // multiprocessors of the current device (cached per device)
 
 cudaError_t launch_fwd_simple(const FwdArgs& a);
+bool tma_path_ok(const FwdArgs& a);       // N == 16, 16-byte aligned rows and pointers, 32-bit row coords
+cudaError_t launch_fwd_tma(const FwdArgs& a);
+int read_and_clear_device_status();       // nonzero if a kernel recorded a failed bounded wait
 cudaError_t launch_init_state(const FwdArgs& a);  // final_state = h0 or 0 (used when L == 0)
 cudaError_t launch_step(const StepArgs& a);
 

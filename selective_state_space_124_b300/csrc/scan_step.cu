@@ -44,17 +44,17 @@ __global__ void __launch_bounds__(256) scan_step_kernel(StepParams p) {
   for (int n = 0; n < NP; ++n) {
     if (!VEC && n >= N) break;
     const float A = -ex2(__ldg(p.A_log + d * N + n) * kLog2e);
-    const float a = ex2(dt * A * kLog2e);
+    const float w = dt * A * kLog2e;
+    const float e = exp2m1(w, ex2(w));  // Abar - 1
     const float bn = Elem<T>::load(p.B, b * N + n);
     const float cn = Elem<T>::load(p.C, b * N + n);
     float bx;
     if (ZOH) {
-      const float e = expm1_small(dt * A, a);
       bx = (A == 0.0f ? dt : e / A) * bn * xv;
     } else {
       bx = dt * bn * xv;
     }
-    h[n] = fmaf(a, h[n], bx);
+    h[n] = fmaf(e, h[n], h[n]) + bx;
     yv = fmaf(cn, h[n], yv);
   }
   if (VEC) {

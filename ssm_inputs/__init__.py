@@ -102,6 +102,16 @@ def workload_inputs(name: str, seed: int = 0, **overrides):
     return inp
 
 
+def token_inputs(batch, D, N, seed=1, mu=-2.0, sigma=1.0, **_):
+    """One decode token's inputs (x_t, delta_t [batch, D]; B_t, C_t [batch, N]), same laws as above."""
+    rng = np.random.default_rng(seed)
+    x = _normal(rng, (batch, D))
+    delta = _softplus_f32(_normal(rng, (batch, D), mu, sigma))
+    B = _normal(rng, (batch, N))
+    C = _normal(rng, (batch, N))
+    return dict(x=x, delta=delta, B=B, C=C)
+
+
 class DecodeStream:
     """Initial state and per-step inputs of the decode workload, drawn lazily in step order."""
 

@@ -198,3 +198,64 @@ def test_workload_long_zoh(orc):
     inp = ssm_inputs.workload_inputs("long")
     cfg = inp["cfg"]
     check_fwd(orc, inp, "f32", "zoh", channels=_sample_channels(cfg["batch"], cfg["D"], 96, 2))
+
+
+# ---- the TMA-staged path (N = 16, 16-byte aligned rows): ragged tiles, short pieces, mixed channels ----
+
+TMA_SHAPES = [
+    # batch, L, D, N
+    (1, 5, 128, 16),        # L shorter than one stage
+    (2, 333, 132, 16),      # ragged channel tile (132 = 128 + 4), ragged stage tail
+    (3, 1234, 260, 16),     # several tiles, pieces crossing rows
+    (1, 50000, 64, 16),     # long: many pieces with a backward carry
+    (8, 4096, 512, 16),     # pieces aligned with rows
+]
+
+
+@pytest.mark.parametrize("shape", TMA_SHAPES, ids=[f"b{s[0]}_L{s[1]}_D{s[2]}" for s in TMA_SHAPES])
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fwd_tma_shapes(orc, shape, disc, dtype):
+    batch, L, D, N = shape
+    if dtype == "bf16" and D % 8:
+        D += 8 - D % 8
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=L + 7 * D, mu=-2.0, sigma=1.0, dtype=dtype)
+    if batch * D <= 512:
+        check_fwd(orc, inp, dtype, disc)
+    else:
+        check_fwd(orc, inp, dtype, disc, channels=_sample_channels(batch, D, 256, L))
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_fwd_tma_mixed_structure(orc, disc):
+    """Some warps' channels have A[d, n] = (n+1) A[d, 0] (the e_n-recurrence path), others do not (the
+    per-entry exp2 path); both in one launch, with an initial state."""
+    batch, L, D, N = 2, 3000, 256, 16
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=21)
+    A_log = ssm_inputs.a_log_s4d(D, N).copy()
+    rng = np.random.default_rng(22)
+    A_log[64:96] = rng.uniform(-1.0, 2.0, (32, N)).astype(np.float32)   # one warp of generic channels
+    A_log[200, 3] += 0.5                                                  # one channel breaks its warp's structure
+    A_log[130, :] += np.float32(np.log(0.25))                            # structured, different A_0
+    inp["A_log"] = A_log
+    h0 = rng.standard_normal((batch, D, N)).astype(np.float32)
+    check_fwd(orc, inp, "f32", disc, h0=h0)
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_fwd_tma_long_memory_and_negative_delta(orc, disc):
+    inp = ssm_inputs.make_inputs(1, 20000, 128, 16, seed=23, mu=-8.0, sigma=1.0)
+    check_fwd(orc, inp, "f32", disc)
+    inp["delta"] = np.random.default_rng(24).uniform(-2e-4, 2e-4, inp["delta"].shape).astype(np.float32)
+    check_fwd(orc, inp, "f32", disc)
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("D", [128, 70])  # 128: TMA path, 70: general path
+def test_fwd_generic_A_long_walks(orc, disc, D):
+    """A without the (n+1) A_0 structure (per-entry exp2 path) over long walks where little decays."""
+    inp = ssm_inputs.make_inputs(1, 30000, D, 16, seed=31, mu=-9.0, sigma=1.0)
+    inp["A_log"] = np.random.default_rng(32).uniform(-2.0, 1.0, (D, 16)).astype(np.float32)
+    check_fwd(orc, inp, "f32", disc)
+    inp["delta"] = np.random.default_rng(33).uniform(-1e-4, 1e-4, inp["delta"].shape).astype(np.float32)
+    check_fwd(orc, inp, "f32", disc)
