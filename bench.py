@@ -1,0 +1,432 @@
+#!/usr/bin/env python
+"""Benchmark of the selective scan's hot path on B300; prints one JSON line (rank 0).
+
+One step = the whole path on one batch of synthetic input: ssm_scan_fwd over the Mamba-130M-shaped
+layer (batch 2, L 2048, D 1536, N 16, fp32, Euler), then one ssm_scan_step continuing from its final
+state (the prefill -> decode hand-off). Units per step: batch * (L + 1) * D scan elements.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Timing: W untimed steps, then K timed steps bracketed by a barrier and a device synchronise; L2 is
+flushed (a 512 MiB write) before every step, outside the CUDA-event pairs that time the step's kernels
+on the launching stream; the job time is the maximum over ranks. Multi-GPU runs (torchrun) are weak
+scaling: every rank scans its own independent batch on its own GPU, with no data-path collective.
+
+--impl reference times the CPU oracle (double precision, OpenMP over channels, as it stands) on the
+host cores: each step is a bounded sample (whole sequences of a subset of the workload's channels).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import ssm_inputs  # noqa: E402
+
+METRIC = "selective-scan B·L·D elems/s; achieved HBM GB/s as fraction of B300 peak"
+FALLBACK_HBM_GBS = 6400.0
+FLUSH_BYTES = 512 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mamba130m",
+                    choices=sorted(k for k in ssm_inputs.WORKLOADS if k != "decode"))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    return ap.parse_args(argv)
+
+
+def describe(name, cfg):
+    return (f"{name}: batch {cfg['batch']}, L {cfg['L']}, D {cfg['D']}, N {cfg['N']}, {cfg['dtype']}, "
+            f"{cfg['disc']}; delta = softplus(N({cfg['mu']}, {cfg['sigma']})), A_log = log(1..N); "
+            f"+ 1 decode step from the final state")
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def fwd_bytes(cfg):
+    """Compulsory bytes of one prefill launch: x, delta, B, C, A_log read; y, final state written."""
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    b, L, D, N = cfg["batch"], cfg["L"], cfg["D"], cfg["N"]
+    return 3 * b * L * D * es + 2 * b * L * N * es + D * N * 4 + b * D * N * 4
+
+
+def step_bytes(cfg):
+    """Compulsory bytes of one decode step: state read + written, x_t, delta_t, y_t, B_t, C_t, A_log."""
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    b, D, N = cfg["batch"], cfg["D"], cfg["N"]
+    return 2 * b * D * N * 4 + 3 * b * D * es + 2 * b * N * es + D * N * 4
+
+
+def ncu_traffic(kernel_prefix, workload):
+    """DRAM bytes per launch from a committed ncu capture, if taken on the current kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    from selective_state_space_124_b300 import build as lib_build
+    entry = rec.get(workload, {})
+    if entry.get("source_hash") != lib_build.source_hash() or not entry.get("kernel", "").startswith(kernel_prefix):
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples the SM clock and clock-event reasons during the timed region (reads only): NVML when the
+    Python bindings are importable, else `nvidia-smi --query-gpu ... -lms 20` as a subprocess."""
+
+    NVML_NAMES = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                  0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+                  0x2: "applications_clocks_setting"}
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.sw_power_cap",
+                  "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                  "clocks_event_reasons.sw_thermal_slowdown"]
+
+    def __init__(self, local_rank):
+        self.local = local_rank
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.mode, self.error = None, None
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = self._nvml_handle(pynvml, local_rank)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.mode = "nvml"
+        except Exception as e:  # noqa: BLE001 -- fall back to nvidia-smi
+            self.error = f"nvml: {type(e).__name__}: {e}"
+            self.mode = "smi"
+
+    @staticmethod
+    def _nvml_handle(nv, local_rank):
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(local_rank)
+            return nv.nvmlDeviceGetHandleByPciBusId(
+                f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0")
+        except Exception:  # noqa: BLE001
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            entry = vis.split(",")[local_rank].strip()
+            if entry.startswith(("GPU-", "MIG-")):
+                return nv.nvmlDeviceGetHandleByUUID(entry)
+            return nv.nvmlDeviceGetHandleByIndex(int(entry))
+        return nv.nvmlDeviceGetHandleByIndex(local_rank)
+
+    def _smi_id(self):
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(self.local)
+            return f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        except Exception:  # noqa: BLE001
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            return vis.split(",")[self.local].strip() if vis else str(self.local)
+
+    def _run_nvml(self):
+        nv = self.nv
+        get_r = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                bits = int(get_r(self.h))
+                self.reasons |= {n for b, n in self.NVML_NAMES.items() if bits & b}
+            except Exception:  # noqa: BLE001
+                pass
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.mode == "nvml":
+            self.t = threading.Thread(target=self._run_nvml, daemon=True)
+            self.t.start()
+        else:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", self._smi_id(), "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                time.sleep(0.3)
+            except Exception as e:  # noqa: BLE001
+                self.proc = None
+                self.error = (self.error or "") + f"; smi: {type(e).__name__}: {e}"
+        return self
+
+    def __exit__(self, *a):
+        if self.mode == "nvml":
+            self._stop.set()
+            self.t.join()
+            return
+        if getattr(self, "proc", None) is None:
+            return
+        time.sleep(0.05)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        names = ["sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+        for line in out.splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) != len(self.SMI_FIELDS):
+                continue
+            try:
+                self.samples.append(float(f[0]))
+                self.max_mhz = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[2:]):
+                if v.lower() == "active":
+                    self.reasons.add(n)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "samples": 0,
+                    "error": self.error}
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.mode}
+
+
+def dist_setup():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank scans its own independent batch (weak scaling): same shapes and laws, seed = rank."""
+    return rank
+
+
+def job_seconds(local_seconds: float, world: int, device=None) -> float:
+    """Job time = the slowest rank's time (max over ranks; the local value when running alone)."""
+    if world <= 1:
+        return local_seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_step: int, steps: int, world: int, seconds: float) -> float:
+    """Whole-job throughput: the units every rank processed, over the job time."""
+    return world * units_per_step * steps / seconds
+
+
+def oracle_sample(inp, cfg, budget_s):
+    """Pick a channel subset whose whole sequences take about budget_s seconds in the oracle."""
+    import oracle
+    orc = oracle.default()
+    total = cfg["batch"] * cfg["D"]
+    n = min(total, max(16, 2 * orc.num_threads()))
+    t0 = time.perf_counter()
+    orc.scan_fwd(inp["x"], inp["delta"], inp["A_log"], inp["B"], inp["C"], disc=cfg["disc"],
+                 channels=list(range(n)))
+    dt = max(time.perf_counter() - t0, 1e-4)
+    n = int(min(total, max(1, n * budget_s / dt)))
+    return list(np.linspace(0, total - 1, n).astype(np.int64))
+
+
+def cpu_oracle_rate(inp, cfg, chans):
+    """Time the oracle on whole sequences of the given channels; returns (elems/s, threads, sample)."""
+    import oracle
+    orc = oracle.default()
+    L, total = cfg["L"], cfg["batch"] * cfg["D"]
+    t0 = time.perf_counter()
+    orc.scan_fwd(inp["x"], inp["delta"], inp["A_log"], inp["B"], inp["C"], disc=cfg["disc"], channels=chans)
+    dt = time.perf_counter() - t0
+    n = len(chans)
+    return n * L / dt, orc.num_threads(), f"{n} of {total} channels, full L = {L} each ({n * L} elems)"
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    cfg = dict(ssm_inputs.WORKLOADS[args.workload])
+    inp = ssm_inputs.workload_inputs(args.workload)
+    chans = oracle_sample(inp, cfg, max(0.02, 120.0 / max(1, args.steps + args.warmup)))
+    rates, cores, sample = [], None, None
+    for i in range(args.warmup + args.steps):
+        r, cores, sample = cpu_oracle_rate(inp, cfg, chans)
+        if i >= args.warmup:
+            rates.append(r)
+    value = float(statistics.median(rates))
+    units = cfg["batch"] * (cfg["L"] + 1) * cfg["D"]
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "elems/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": units / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": describe(args.workload, cfg), "l2": "n/a (host)"},
+        "cpu_baseline": {"value": value, "unit": "elems/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + sample},
+        "e2e": {"value": value, "unit": "elems/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, rank)
+
+    import torch
+    import torch.distributed as dist
+
+    import selective_state_space_124_b300 as lib
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+
+    cfg = dict(ssm_inputs.WORKLOADS[args.workload])
+    inp = ssm_inputs.workload_inputs(args.workload, seed=rank_seed(rank))
+    tok = ssm_inputs.token_inputs(cfg["batch"], cfg["D"], cfg["N"], seed=1000 + rank_seed(rank),
+                                  mu=cfg["mu"], sigma=cfg["sigma"])
+    bf16 = cfg["dtype"] == "bf16"
+    tdt = torch.bfloat16 if bf16 else torch.float32
+
+    def host_tensor(a):
+        if bf16:
+            return torch.from_numpy(ssm_inputs.bf16_round(a).view(np.int16).copy()).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32))
+
+    hx = {k: host_tensor(inp[k]).pin_memory() for k in ("x", "delta", "B", "C")}
+    hx["A_log"] = torch.from_numpy(inp["A_log"].copy()).pin_memory()
+    ht = {k: host_tensor(tok[k]).pin_memory() for k in ("x", "delta", "B", "C")}
+    dev = {k: v.cuda() for k, v in hx.items()}
+    dtok = {k: v.cuda() for k, v in ht.items()}
+    b, L, D, N = cfg["batch"], cfg["L"], cfg["D"], cfg["N"]
+    y = torch.empty((b, L, D), dtype=tdt, device="cuda")
+    state = torch.empty((b, D, N), dtype=torch.float32, device="cuda")
+    y_t = torch.empty((b, D), dtype=tdt, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        lib.ssm_scan_fwd(dev["x"], dev["delta"], dev["A_log"], dev["B"], dev["C"], disc=cfg["disc"], y=y,
+                         final_state=state)
+
+    def step():
+        lib.ssm_scan_step(state, dtok["x"], dtok["delta"], dev["A_log"], dtok["B"], dtok["C"], disc=cfg["disc"],
+                          y_t=y_t)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        fwd()
+        step()
+    lib.check_device()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    with sampler:
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            step()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    lib.check_device()
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    stp_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    total_s = job_seconds((sum(fwd_ms) + sum(stp_ms)) / 1e3, world, device="cuda")
+    units_step = b * (L + 1) * D
+    value = job_value(units_step, K, world, total_s)
+
+    # ---- end to end through the public API: pinned host inputs in, results back to the host ------------
+    e2e = None
+    if not args.no_e2e:
+        hy = torch.empty((b, L, D), dtype=tdt).pin_memory()
+        hs = torch.empty((b, D, N), dtype=torch.float32).pin_memory()
+        hyt = torch.empty((b, D), dtype=tdt).pin_memory()
+        KE = max(3, min(K, 200))
+        eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KE)]
+        h2d = sum(t.numel() * t.element_size() for t in list(hx.values()) + list(ht.values()))
+        d2h = sum(t.numel() * t.element_size() for t in (hy, hs, hyt))
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(KE):
+            flush.zero_()
+            eve[i][0].record(stream)
+            for k in hx:
+                dev[k].copy_(hx[k], non_blocking=True)
+            for k in ht:
+                dtok[k].copy_(ht[k], non_blocking=True)
+            fwd()
+            step()
+            hy.copy_(y, non_blocking=True)
+            hs.copy_(state, non_blocking=True)
+            hyt.copy_(y_t, non_blocking=True)
+            eve[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_s = job_seconds(sum(e[0].elapsed_time(e[1]) for e in eve) / 1e3, world, device="cuda")
+        e2e = {"value": job_value(units_step, KE, world, e2e_s), "unit": "elems/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": KE}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    fwd_avg_s = statistics.mean(fwd_ms) / 1e3
+    achieved = fwd_bytes(cfg) / fwd_avg_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "elems/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_s / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg["dtype"], "data": "synthetic",
+        "config": {"workload": describe(args.workload, cfg), "l2": "flushed (512 MiB write) before every step",
+                   "parallelism": f"weak x{world}: one independent batch per GPU (seed = rank), no collective"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic("scan_fwd", args.workload),
+                     "peak_kind": peak_kind, "kernel": "ssm_scan_fwd",
+                     "algorithmic_bytes_per_launch": fwd_bytes(cfg), "avg_launch_ms": fwd_avg_s * 1e3},
+        "fwd_ms_median": statistics.median(fwd_ms), "step_ms_median": statistics.median(stp_ms),
+        "step_kernel_gbs": step_bytes(cfg) / (statistics.mean(stp_ms) / 1e3) / 1e9,
+        "wall_s_timed_region": wall,
+        "clocks": sampler.summary(),
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+    }
+    if not args.no_cpu_baseline:
+        r, cores, sample = cpu_oracle_rate(inp, cfg, oracle_sample(inp, cfg, args.cpu_seconds))
+        line["cpu_baseline"] = {"value": r, "unit": "elems/s", "cores": cores, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,62 @@
+"""Host logic of multi-GPU benchmark runs, exercised with two gloo ranks on the CPU: every rank scans its
+own batch (seed = rank, weak scaling), the job time is the slowest rank's, the value counts all ranks'
+units, and no collective touches the data path."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    import ssm_inputs
+    local = [0.5, 2.0][rank]
+    t = bench.job_seconds(local, world, device="cpu")
+    v = bench.job_value(1000, 10, world, t)
+    inp = ssm_inputs.workload_inputs("tiny", seed=bench.rank_seed(rank))
+    out[rank] = (t, v, float(inp["x"].reshape(-1)[0]))
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_max_time_and_independent_batches():
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    t0, v0, x0 = out[0]
+    t1, v1, x1 = out[1]
+    assert t0 == t1 == 2.0                      # slowest rank
+    assert v0 == v1 == pytest.approx(2 * 1000 * 10 / 2.0)
+    assert x0 != x1                             # different seeds: independent batches
+
+
+def test_single_rank_needs_no_process_group():
+    import bench
+    assert bench.job_seconds(1.5, 1) == 1.5
+    assert bench.job_value(10, 3, 1, 1.5) == 20.0
+
+
+def test_reference_arm_line(capsys):
+    """--impl reference prints the contract's JSON line from the oracle alone (tiny workload)."""
+    import json
+    import bench
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "elems/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
