@@ -324,13 +324,20 @@ def main(argv=None):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
+    # The timed loop calls the C ABI on precomputed device addresses: launching costs a few microseconds of
+    # host time, well under the L2 flush that precedes every step, so the host stays ahead of the device and
+    # the event pairs measure kernel time only (the e2e leg below goes through the tensor-level binding).
+    sh = stream.cuda_stream
+    fwd_args = (dev["x"].data_ptr(), dev["delta"].data_ptr(), dev["A_log"].data_ptr(), dev["B"].data_ptr(),
+                dev["C"].data_ptr(), 0, y.data_ptr(), state.data_ptr(), b, L, D, N, cfg["dtype"], cfg["disc"], sh)
+    step_args = (state.data_ptr(), dtok["x"].data_ptr(), dtok["delta"].data_ptr(), dev["A_log"].data_ptr(),
+                 dtok["B"].data_ptr(), dtok["C"].data_ptr(), y_t.data_ptr(), b, D, N, cfg["dtype"], cfg["disc"], sh)
+
     def fwd():
-        lib.ssm_scan_fwd(dev["x"], dev["delta"], dev["A_log"], dev["B"], dev["C"], disc=cfg["disc"], y=y,
-                         final_state=state)
+        lib.ssm_scan_fwd_ptr(*fwd_args)
 
     def step():
-        lib.ssm_scan_step(state, dtok["x"], dtok["delta"], dev["A_log"], dtok["B"], dtok["C"], disc=cfg["disc"],
-                          y_t=y_t)
+        lib.ssm_scan_step_ptr(*step_args)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -344,8 +351,10 @@ def main(argv=None):
         dist.barrier()
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
+    head = torch.empty(4 * FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     with sampler:
         wall0 = time.perf_counter()
+        head.zero_()  # a long first write: the host enqueues ahead of the device from the start
         for i in range(K):
             flush.zero_()
             ev[i][0].record(stream)
