@@ -10,7 +10,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // Decay products below this bound end the backward reconstruction of a segment's initial state:
 // the omitted remainder is at most kCarryEps * |state| at the stopping point.
-constexpr float kCarryEps = 1.4901161193847656e-08f;  // 2^-26
+constexpr float kCarryEps = 9.5367431640625e-07f;  // 2^-20
 
 // 2^x with the SFU approximation (denormal results flush to zero).
 __device__ __forceinline__ float ex2(float x) {
@@ -19,13 +19,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^w - 1 with no cancellation for small |w| (w = delta * A * log2(e)): Taylor series in w (coefficients
-// ln2^k / k!) for |w ln 2| < 1/32 (remainder below 1e-8 relative), else a - 1 with a the SFU value of
-// 2^w. Applying a decay as h + (2^w - 1) h keeps the factor exact to one rounding even when nothing decays
-// for many steps (the SFU value's tiny bias near 1 would otherwise accumulate).
+// 2^w - 1 with no cancellation for small |w| (w = delta * A * log2(e)). For |w ln 2| < 1/32 the Taylor
+// series to the cubic term (coefficients ln2^k / k!) is used: its remainder is below 4e-8 absolute, under the
+// fp32 spacing of 1 + e, so the decay factor 1 + e stays exact to one rounding even when nothing decays for
+// many steps. Above that bound a - 1, with a the SFU value of 2^w, has a relative error below 1e-5 and
+// no accumulation problem (such entries forget within 32 steps).
 __device__ __forceinline__ float exp2m1(float w, float a) {
-  float q = fmaf(w, 0.009618129107628477f, 0.05550410866482158f);
-  q = fmaf(w, q, 0.2402265069591007f);
+  float q = fmaf(w, 0.05550410866482158f, 0.2402265069591007f);
   q = fmaf(w, q, 0.6931471805599453f);
   q *= w;
   return fabsf(w) < 0.04508422002825452f ? q : a - 1.0f;

@@ -11,8 +11,9 @@
 // Carry without communication. A range that starts at t0 > 0 rebuilds the state entering t0 by walking
 // the preceding steps backwards and summing prod_{k>j} Abar_k * Bbar_j x_j ("Mathematical Prerequisites
 // for Mamba" s6, the unrolled sum of the recurrence), to t = 0 (exact) or until the decay product of an
-// entry falls below 2^-26 for every lane of the warp: the omitted remainder of that entry is then at most
-// 2^-26 of its state at that point. For the S4D-structured A (A_n = (n + 1) A_0) the entries decay at
+// entry falls below 2^-20 for every lane of the warp: the omitted remainder of that entry is then at most
+// 2^-20 (under 1e-6) of its state at that point, about the rounding noise a long fp32 recurrence carries
+// anyway. For the S4D-structured A (A_n = (n + 1) A_0) the entries decay at
 // rates 1..16 x A_0, so the walk drops state pairs as they die (8 -> 4 -> 2 -> 1 pairs active): the
 // warm-up costs about a quarter of a full walk.
 //
@@ -36,6 +37,8 @@
 //  * y = sum_n C_n h_n.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -50,20 +53,21 @@ __device__ int g_device_status = 0;  // nonzero: a bounded wait ran out (read by
 namespace {
 
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any single mbarrier wait
-constexpr float kDeadLog2 = -26.0f;                      // log2 of the decay bound that ends a warm-up
+constexpr float kDeadLog2 = -20.0f;                      // log2 of the decay bound that ends a warm-up
 
-template <typename T, int CPL, int TS, int NSF, int NSW>
+template <typename T, int CPL, int TS, int NSF, int TSW, int NSW>
 struct alignas(128) WarpRing {
   static constexpr int CW = 32 * CPL;  // channels per warp
   T fx[NSF][TS * CW];   // forward ring: x, delta tiles [TS][CW]
   T fd[NSF][TS * CW];
   T fB[NSF][TS * 16];   // B, C tiles [TS][16]
   T fC[NSF][TS * 16];
-  T wx[NSW][TS * CW];   // warm-up ring: x, delta, B tiles
-  T wd[NSW][TS * CW];
-  T wB[NSW][TS * 16];
-  float Bf[TS * 16];    // B of the stage being consumed, widened / pre-scaled (bf16 or ZOH)
-  float Cf[TS * 16];    // C of the stage being consumed, widened (bf16)
+  T wx[NSW][TSW * CW];  // warm-up ring: x, delta, B tiles of TSW steps
+  T wd[NSW][TSW * CW];
+  T wB[NSW][TSW * 16];
+  static constexpr int kConvRows = sizeof(T) == 2 ? TS : 2;  // only bf16 inputs need the widened copy
+  float Bf[kConvRows * 16];  // B of the stage being consumed, widened to fp32 (bf16 inputs)
+  float Cf[kConvRows * 16];  // C of the stage being consumed, widened to fp32 (bf16 inputs)
   unsigned long long fbar[NSF];
   unsigned long long wbar[NSW];
 };
@@ -145,6 +149,11 @@ template <> __device__ __forceinline__ float tof<__nv_bfloat16>(__nv_bfloat16 v)
 __device__ __forceinline__ void store_y(float* p, float v, bool pred) {
   asm volatile("{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q st.global.cs.f32 [%0], %1;\n}\n"
                ::"l"(p), "f"(v), "r"(static_cast<int>(pred)));
+}
+__device__ __forceinline__ void store_y(float* p, float v) { asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v)); }
+__device__ __forceinline__ void store_y(__nv_bfloat16* p, float v) {
+  const unsigned short bits = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p), "h"(bits));
 }
 __device__ __forceinline__ void store_y(__nv_bfloat16* p, float v, bool pred) {
   const unsigned short bits = __bfloat16_as_ushort(__float2bfloat16_rn(v));
@@ -302,20 +311,24 @@ __device__ __forceinline__ void fwd_s4d(const float (&xv)[CPL], const float (&dv
   const float4* Bq = reinterpret_cast<const float4*>(Brow);
   const float4* Cq = reinterpret_cast<const float4*>(Crow);
   float2 e[CPL][8];
-  float2 s[CPL];  // per channel: x / A_0 (ZOH; B rows are pre-scaled by 1/(n+1)) or delta * x (Euler)
+  float2 s[CPL];  // per channel: x / A_0 (ZOH) or delta * x (Euler)
 #pragma unroll
   for (int c = 0; c < CPL; ++c) {
     const float w = dv[c] * A2_0[c];
     em1_tree<8>(exp2m1(w, ex2(w)), e[c]);
     s[c] = bc2(ZOH ? xv[c] * invA0[c] : dv[c] * xv[c]);
   }
-  float2 ya[CPL], yb[CPL];
+  float2 ya[CPL];
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) ya[c] = yb[c] = make_float2(0.0f, 0.0f);
+  for (int c = 0; c < CPL; ++c) ya[c] = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const float4 bb = Bq[q], cc = Cq[q];
-    const float2 b0 = make_float2(bb.x, bb.y), b1 = make_float2(bb.z, bb.w);
+    float2 b0 = make_float2(bb.x, bb.y), b1 = make_float2(bb.z, bb.w);
+    if (ZOH) {  // B_n / (n + 1), shared by the CPL channels of the lane
+      b0 = __fmul2_rn(b0, make_float2(1.0f / static_cast<float>(4 * q + 1), 1.0f / static_cast<float>(4 * q + 2)));
+      b1 = __fmul2_rn(b1, make_float2(1.0f / static_cast<float>(4 * q + 3), 1.0f / static_cast<float>(4 * q + 4)));
+    }
     const float2 c0 = make_float2(cc.x, cc.y), c1 = make_float2(cc.z, cc.w);
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
@@ -329,11 +342,11 @@ __device__ __forceinline__ void fwd_s4d(const float (&xv)[CPL], const float (&dv
         h1 = __ffma2_rn(s[c], b1, __ffma2_rn(e[c][2 * q + 1], h1, h1));
       }
       ya[c] = __ffma2_rn(c0, h0, ya[c]);
-      yb[c] = __ffma2_rn(c1, h1, yb[c]);
+      ya[c] = __ffma2_rn(c1, h1, ya[c]);
     }
   }
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) y[c] = (ya[c].x + ya[c].y) + (yb[c].x + yb[c].y);
+  for (int c = 0; c < CPL; ++c) y[c] = ya[c].x + ya[c].y;
 }
 
 template <bool ZOH>
@@ -353,16 +366,291 @@ __device__ __forceinline__ float fwd_gen(float xv, float dv, const float* Brow, 
   return (ya.x + ya.y) + (yb.x + yb.y);
 }
 
-template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int NSW>
+// Shared state of one warp's pipelines.
+struct WarpPipe {
+  uint32_t cseq;        // forward stages consumed
+  uint32_t wiss, wcon;  // warm-up stages issued / consumed (over the warp's lifetime)
+};
+
+// Start of a warm-up walk into t0 > 0: wait for the copies a previous walk left in flight, then issue the
+// first NSW tiles (before the caller's global loads of A_log, so their latency overlaps). Returns the number
+// of tiles issued (all lanes), or -1 if a wait ran out.
+template <typename T, int CPL, int TS, int NSF, int TSW, int NSW>
+__device__ __forceinline__ int warm_prologue(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r, const CUtensorMap* mx,
+                                             const CUtensorMap* md, const CUtensorMap* mB, int lane, int64_t trow0,
+                                             int col, int64_t t0, WarpPipe& wp) {
+  constexpr int CW = 32 * CPL;
+  constexpr uint32_t kWarmBytes = (2u * TSW * CW + TSW * 16) * sizeof(T);
+  while (wp.wcon < wp.wiss) {
+    if (!mbar_wait(&r.wbar[wp.wcon % NSW], (wp.wcon / NSW) & 1u)) return -1;
+    ++wp.wcon;
+  }
+  int kiss = 0;
+#pragma unroll 1
+  for (int i = 0; i < NSW; ++i) {
+    const int64_t thi = t0 - static_cast<int64_t>(kiss) * TSW;
+    if (thi <= 0) break;
+    const int64_t tlo = thi - TSW > 0 ? thi - TSW : 0;
+    if (lane == 0) {
+      const int slot = static_cast<int>(wp.wiss % NSW);
+      const int trow = static_cast<int>(trow0 + tlo);
+      mbar_arrive_tx(&r.wbar[slot], kWarmBytes);
+      tma_load(r.wx[slot], mx, col, trow, &r.wbar[slot]);
+      tma_load(r.wd[slot], md, col, trow, &r.wbar[slot]);
+      tma_load(r.wB[slot], mB, 0, trow, &r.wbar[slot]);
+    }
+    ++kiss;
+    ++wp.wiss;
+  }
+  __syncwarp();
+  return kiss;
+}
+
+// One piece of a warp's range: row (batch b, channel group), steps [t0, t1). Warm-up (t0 > 0), forward with
+// y stores, final state (t1 == L). S4D selects the structured-A arithmetic at compile time, so the two
+// paths do not hold each other's per-channel constants in registers. Returns false if a wait ran out.
+template <bool S4D, typename T, bool ZOH, int CPL, int TS, int NSF, int TSW, int NSW, typename IssueFwd>
+__device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r, const TmaParams& p,
+                                          const CUtensorMap* mx, const CUtensorMap* md, const CUtensorMap* mB,
+                                          int lane, int64_t row, int64_t t0, int64_t t1, WarpPipe& wp,
+                                          IssueFwd& issue_fwd, int kiss0) {
+  constexpr int CW = 32 * CPL;
+  constexpr bool kConv = sizeof(T) == 2;  // bf16: consumers read B and C from the widened Bf / Cf
+  constexpr uint32_t kWarmBytes = (2u * TSW * CW + TSW * 16) * sizeof(T);
+  const int64_t L = p.L;
+  const int64_t b = row / p.G;
+  const int64_t d0 = (row % p.G) * CW + lane;  // channel c of this lane is d0 + 32 c
+  bool act[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) act[c] = d0 + 32 * c < p.D;
+  const bool full = (row % p.G) * CW + CW <= p.D;  // every channel of the warp exists
+
+  // ---- per-channel constants ----
+  float A2_0[CPL], invA0[CPL];  // structured: A_0 log2(e), 1 / A_0
+  ChanGen g[S4D ? 1 : CPL];     // generic: every entry's rate
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const int64_t d = d0 + 32 * c;
+    if constexpr (S4D) {
+      const float A0 = act[c] ? -expf(__ldg(p.A_log + d * 16)) : -1.0f;
+      A2_0[c] = A0 * kLog2e;
+      invA0[c] = 1.0f / A0;
+    } else {
+      ChanGen& gc = g[S4D ? 0 : c];
+      gc.A2max = -3.0e38f;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        const float A = act[c] ? -expf(__ldg(p.A_log + d * 16 + n)) : -static_cast<float>(n + 1);
+        gc.A2[n] = A * kLog2e;
+        gc.invA[n] = A == 0.0f ? 0.0f : 1.0f / A;
+        gc.A2max = fmaxf(gc.A2max, gc.A2[n]);
+      }
+    }
+  }
+
+  float2 h[CPL][8];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[c][k] = make_float2(0.0f, 0.0f);
+  const float* h0row[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) h0row[c] = (p.h0 && act[c]) ? p.h0 + (b * p.D + d0 + 32 * c) * 16 : nullptr;
+
+  if (t0 == 0) {
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      if (h0row[c]) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 v = reinterpret_cast<const float4*>(h0row[c])[k];
+          h[c][2 * k] = make_float2(v.x, v.y);
+          h[c][2 * k + 1] = make_float2(v.z, v.w);
+        }
+      }
+    }
+  } else {
+    // ---- state entering t0: backward walk over warm-up tiles (the first NSW were issued by the caller) ----
+    int kiss = kiss0;  // warm-up tiles issued for this walk (tile k covers [max(t0 - (k+1) TSW, 0), t0 - k TSW))
+    const int col = static_cast<int>((row % p.G) * CW);
+    auto issue_warm = [&]() {
+      const int64_t thi = t0 - static_cast<int64_t>(kiss) * TSW;
+      if (thi <= 0) return;
+      const int64_t tlo = thi - TSW > 0 ? thi - TSW : 0;
+      const int slot = static_cast<int>(wp.wiss % NSW);
+      const int trow = static_cast<int>(b * L + tlo);
+      mbar_arrive_tx(&r.wbar[slot], kWarmBytes);
+      tma_load(r.wx[slot], mx, col, trow, &r.wbar[slot]);
+      tma_load(r.wd[slot], md, col, trow, &r.wbar[slot]);
+      tma_load(r.wB[slot], mB, 0, trow, &r.wbar[slot]);
+      ++kiss;
+      ++wp.wiss;
+    };
+
+    float2 P[CPL][8];
+    float W[CPL];  // structured: log2 decay of entry 0 over the steps walked; generic: sum of delta
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      W[c] = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) P[c][k] = make_float2(1.0f, 1.0f);
+    }
+    int np = 8;  // structured: state pairs still accumulating
+    for (int k = 0;; ++k) {
+      const int64_t thi = t0 - static_cast<int64_t>(k) * TSW;
+      const int64_t tlo = thi - TSW > 0 ? thi - TSW : 0;
+      const int n = static_cast<int>(thi - tlo);
+      const int slot = static_cast<int>(wp.wcon % NSW);
+      if (!mbar_wait(&r.wbar[slot], (wp.wcon / NSW) & 1u)) return false;
+      const T* xs = r.wx[slot];
+      const T* ds = r.wd[slot];
+      const T* Bs = r.wB[slot];
+      if constexpr (S4D) {
+        if (np == 8) warm_s4d<8, ZOH, CPL, TSW>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
+        else if (np == 4) warm_s4d<4, ZOH, CPL, TSW>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
+        else if (np == 2) warm_s4d<2, ZOH, CPL, TSW>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
+        else warm_s4d<1, ZOH, CPL, TSW>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
+      } else {
+        warm_gen<ZOH, CPL>(xs, ds, Bs, n, lane, g, W, P, h);
+      }
+      ++wp.wcon;
+      // Pair k holds entries 2k, 2k+1 whose log2 decay is (2k+1) W, (2k+2) W (structured). A pair is
+      // dropped once its slower entry has decayed below 2^-20 on every active channel; dropping is final.
+      float wl = -3.0e38f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c)
+        if (act[c]) wl = fmaxf(wl, S4D ? W[c] : W[c] * g[S4D ? 0 : c].A2max);
+      const float wmax = warp_max(wl);
+      const bool at_start = (tlo == 0);
+      bool done;
+      if (S4D) {
+        // pair k is live while (2k+1) * wmax > kDeadLog2 (monotone in k); np shrinks to the smallest of
+        // 8, 4, 2, 1, 0 that keeps every live pair.
+        int live = 0;
+        if (wmax > kDeadLog2 / 15.0f) live = 8;
+        else if (wmax > kDeadLog2 / 13.0f) live = 7;
+        else if (wmax > kDeadLog2 / 11.0f) live = 6;
+        else if (wmax > kDeadLog2 / 9.0f) live = 5;
+        else if (wmax > kDeadLog2 / 7.0f) live = 4;
+        else if (wmax > kDeadLog2 / 5.0f) live = 3;
+        else if (wmax > kDeadLog2 / 3.0f) live = 2;
+        else if (wmax > kDeadLog2) live = 1;
+        const int want = live > 4 ? 8 : live > 2 ? 4 : live;  // 8, 4, 2, 1 or 0
+        if (want < np) np = want;
+        done = at_start || np == 0;
+      } else {
+        done = at_start || wmax <= kDeadLog2;
+      }
+      if (done) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          if (ZOH && S4D) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              h[c][q] = __fmul2_rn(h[c][q], make_float2(1.0f / static_cast<float>(2 * q + 1),
+                                                        1.0f / static_cast<float>(2 * q + 2)));
+          }
+          if (at_start && h0row[c]) {
+            // plus (decay over [0, t0)) * h0 for the entries still live (dropped ones decayed below 2^-20)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 v = reinterpret_cast<const float4*>(h0row[c])[q];
+              if (!S4D || 2 * q < np) h[c][2 * q] = __ffma2_rn(P[c][2 * q], make_float2(v.x, v.y), h[c][2 * q]);
+              if (!S4D || 2 * q + 1 < np)
+                h[c][2 * q + 1] = __ffma2_rn(P[c][2 * q + 1], make_float2(v.z, v.w), h[c][2 * q + 1]);
+            }
+          }
+        }
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) issue_warm();
+    }
+  }
+
+  // ---- forward over [t0, t1) ----
+  for (int64_t tb = t0; tb < t1; tb += TS) {
+    const int n = static_cast<int>((t1 - tb) < TS ? (t1 - tb) : TS);
+    const int slot = static_cast<int>(wp.cseq % NSF);
+    if (!mbar_wait(&r.fbar[slot], (wp.cseq / NSF) & 1u)) return false;
+    const T* xs = r.fx[slot];
+    const T* ds = r.fd[slot];
+    if (kConv) {
+#pragma unroll
+      for (int j = 0; j < TS * 16 / 32; ++j) {
+        const int i = lane + 32 * j;
+        r.Bf[i] = tof<T>(r.fB[slot][i]);
+        r.Cf[i] = tof<T>(r.fC[slot][i]);
+      }
+      __syncwarp();
+    }
+    const float* Bs = kConv ? r.Bf : reinterpret_cast<const float*>(r.fB[slot]);
+    const float* Cs = kConv ? r.Cf : reinterpret_cast<const float*>(r.fC[slot]);
+    T* yp = static_cast<T*>(p.y) + (b * L + tb) * p.D + d0;  // channel c at yp + 32 c
+    if constexpr (S4D) {
+      auto one = [&](auto all_active, int i) {
+        float xv[CPL], dv[CPL], yv[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          xv[c] = tof<T>(xs[i * CW + c * 32 + lane]);
+          dv[c] = tof<T>(ds[i * CW + c * 32 + lane]);
+        }
+        fwd_s4d<ZOH, CPL>(xv, dv, Bs + i * 16, Cs + i * 16, A2_0, invA0, h, yv);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          if constexpr (decltype(all_active)::value) store_y(yp + 32 * c, yv[c]);
+          else store_y(yp + 32 * c, yv[c], act[c]);
+        }
+        yp += p.D;
+      };
+      if (n == TS && full) {
+#pragma unroll
+        for (int i = 0; i < TS; ++i) one(std::true_type{}, i);
+      } else if (n == TS) {
+#pragma unroll
+        for (int i = 0; i < TS; ++i) one(std::false_type{}, i);
+      } else {
+#pragma unroll 1
+        for (int i = 0; i < n; ++i) one(std::false_type{}, i);
+      }
+    } else {
+#pragma unroll 1
+      for (int i = 0; i < n; ++i) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          const float yv = fwd_gen<ZOH>(tof<T>(xs[i * CW + c * 32 + lane]), tof<T>(ds[i * CW + c * 32 + lane]),
+                                        Bs + i * 16, Cs + i * 16, g[S4D ? 0 : c], h[c]);
+          store_y(yp + 32 * c, yv, act[c]);
+        }
+        yp += p.D;
+      }
+    }
+    __syncwarp();
+    ++wp.cseq;
+    if (lane == 0) issue_fwd();
+  }
+  if (t1 == L && p.final_state) {
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      if (!act[c]) continue;
+      float4* fs = reinterpret_cast<float4*>(p.final_state + (b * p.D + d0 + 32 * c) * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        fs[q] = make_float4(h[c][2 * q].x, h[c][2 * q].y, h[c][2 * q + 1].x, h[c][2 * q + 1].y);
+    }
+  }
+  return true;
+}
+
+template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int TSW, int NSW>
 __global__ void __launch_bounds__(NW * 32, 1)
 scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap md,
-                    const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mC, TmaParams p) {
-  using R = WarpRing<T, CPL, TS, NSF, NSW>;
+                    const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mC,
+                    const __grid_constant__ CUtensorMap mxw, const __grid_constant__ CUtensorMap mdw,
+                    const __grid_constant__ CUtensorMap mBw, TmaParams p) {
+  using R = WarpRing<T, CPL, TS, NSF, TSW, NSW>;
   constexpr int CW = R::CW;
-  constexpr bool kConvB = ZOH || sizeof(T) == 2;  // consumers read B from Bf
-  constexpr bool kConvC = sizeof(T) == 2;         // consumers read C from Cf
   constexpr uint32_t kFwdBytes = (2u * TS * CW + 2u * TS * 16) * sizeof(T);
-  constexpr uint32_t kWarmBytes = (2u * TS * CW + TS * 16) * sizeof(T);
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -384,281 +672,79 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
   const int64_t L = p.L;
 
   // Forward stages, in the order the consumer takes them: the range [lo0, hi0) cut at row ends and every
-  // TS steps. Lane 0 issues them NSF ahead of consumption.
+  // TS steps. Lane 0 issues them NSF ahead of consumption. The cursor advances without divisions (64-bit
+  // division is a long software sequence).
   int64_t ipos = lo0;   // first step of the next forward stage to issue
   uint32_t iseq = 0;    // forward stages issued
+  int64_t it = lo0 % L, ib = (lo0 / L) / p.G, ig = (lo0 / L) % p.G;  // its step, batch, channel group
   auto issue_fwd = [&]() {
     if (ipos >= hi0) return;
-    const int64_t row = ipos / L, t = ipos % L;
-    const int64_t room = (L - t) < (hi0 - ipos) ? (L - t) : (hi0 - ipos);
+    const int64_t room = (L - it) < (hi0 - ipos) ? (L - it) : (hi0 - ipos);
     const int64_t n = room < TS ? room : TS;
     const int slot = static_cast<int>(iseq % NSF);
-    const int64_t b = row / p.G, g = row % p.G;
-    const int trow = static_cast<int>(b * L + t);
-    const int col = static_cast<int>(g * CW);
+    const int trow = static_cast<int>(ib * L + it);
+    const int col = static_cast<int>(ig * CW);
     mbar_arrive_tx(&r.fbar[slot], kFwdBytes);
     tma_load(r.fx[slot], &mx, col, trow, &r.fbar[slot]);
     tma_load(r.fd[slot], &md, col, trow, &r.fbar[slot]);
     tma_load(r.fB[slot], &mB, 0, trow, &r.fbar[slot]);
     tma_load(r.fC[slot], &mC, 0, trow, &r.fbar[slot]);
     ipos += n;
+    it += n;
+    if (it == L) {
+      it = 0;
+      if (++ig == p.G) {
+        ig = 0;
+        ++ib;
+      }
+    }
     ++iseq;
   };
   if (lane == 0)
     for (int i = 0; i < NSF; ++i) issue_fwd();
 
-  uint32_t cseq = 0;              // forward stages consumed
-  uint32_t wiss = 0, wcon = 0;    // warm-up stages issued / consumed (over the warp's lifetime)
-  bool alive = true;
-
+  WarpPipe wp{0u, 0u, 0u};
   int64_t lo = lo0;
-  while (lo < hi0 && alive) {
+  while (lo < hi0) {
     const int64_t row = lo / L, t0 = lo % L;
     const int64_t t1 = (hi0 - lo < L - t0) ? t0 + (hi0 - lo) : L;
     lo += t1 - t0;
-    const int64_t b = row / p.G;
-    const int64_t d0 = (row % p.G) * CW + lane;  // channel c of this lane is d0 + 32 c
-    bool act[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) act[c] = d0 + 32 * c < p.D;
-
-    // ---- channel constants; S4D structure check (warp-uniform) ----
-    float A2_0[CPL], invA0[CPL];
-    ChanGen g[CPL];
+    int kiss0 = 0;
+    if (t0 > 0) {
+      kiss0 = warm_prologue(r, &mxw, &mdw, &mBw, lane, (row / p.G) * L, static_cast<int>((row % p.G) * CW), t0, wp);
+      if (kiss0 < 0) break;
+    }
+    // S4D structure check (warp-uniform): A[d, n] = (n + 1) A[d, 0] for every channel of the warp.
+    const int64_t d0 = (row % p.G) * CW + lane;
     bool ok = true;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
-      float Araw[16];
       const int64_t d = d0 + 32 * c;
+      if (d < p.D) {
+        const float A0 = -expf(__ldg(p.A_log + d * 16));
+        bool okc = A0 < -1e-30f && A0 > -3.0e38f;
 #pragma unroll
-      for (int n = 0; n < 16; ++n)
-        Araw[n] = act[c] ? -expf(__ldg(p.A_log + d * 16 + n)) : -static_cast<float>(n + 1);
-      bool okc = Araw[0] < -1e-30f && Araw[0] > -3.0e38f;
-#pragma unroll
-      for (int n = 1; n < 16; ++n)
-        okc = okc && fabsf(Araw[n] - static_cast<float>(n + 1) * Araw[0]) <= 4.8e-7f * fabsf(Araw[n]);
-      ok = ok && okc;
-      A2_0[c] = Araw[0] * kLog2e;
-      invA0[c] = 1.0f / Araw[0];
-      g[c].A2max = -3.0e38f;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        g[c].A2[n] = Araw[n] * kLog2e;
-        g[c].invA[n] = Araw[n] == 0.0f ? 0.0f : 1.0f / Araw[n];
-        g[c].A2max = fmaxf(g[c].A2max, g[c].A2[n]);
+        for (int n = 1; n < 16; ++n) {
+          const float A = -expf(__ldg(p.A_log + d * 16 + n));
+          okc = okc && fabsf(A - static_cast<float>(n + 1) * A0) <= 4.8e-7f * fabsf(A);
+        }
+        ok = ok && okc;
       }
     }
-    const bool s4d = __all_sync(0xffffffffu, ok);
-
-    float2 h[CPL][8];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c)
-#pragma unroll
-      for (int k = 0; k < 8; ++k) h[c][k] = make_float2(0.0f, 0.0f);
-    const float* h0row[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) h0row[c] = (p.h0 && act[c]) ? p.h0 + (b * p.D + d0 + 32 * c) * 16 : nullptr;
-
-    if (t0 == 0) {
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        if (h0row[c]) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float4 v = reinterpret_cast<const float4*>(h0row[c])[k];
-            h[c][2 * k] = make_float2(v.x, v.y);
-            h[c][2 * k + 1] = make_float2(v.z, v.w);
-          }
-        }
-      }
-    } else {
-      // ---- state entering t0: backward walk over warm-up tiles ----
-      while (wcon < wiss) {  // copies left in flight by the previous walk
-        if (!mbar_wait(&r.wbar[wcon % NSW], (wcon / NSW) & 1u)) { alive = false; break; }
-        ++wcon;
-      }
-      if (!alive) break;
-      int kiss = 0;  // warm-up tiles issued for this walk (tile k covers [max(t0 - (k+1) TS, 0), t0 - k TS))
-      auto issue_warm = [&]() {
-        const int64_t thi = t0 - static_cast<int64_t>(kiss) * TS;
-        if (thi <= 0) return;
-        const int64_t tlo = thi - TS > 0 ? thi - TS : 0;
-        const int slot = static_cast<int>(wiss % NSW);
-        const int trow = static_cast<int>(b * L + tlo);
-        const int col = static_cast<int>((row % p.G) * CW);
-        mbar_arrive_tx(&r.wbar[slot], kWarmBytes);
-        tma_load(r.wx[slot], &mx, col, trow, &r.wbar[slot]);
-        tma_load(r.wd[slot], &md, col, trow, &r.wbar[slot]);
-        tma_load(r.wB[slot], &mB, 0, trow, &r.wbar[slot]);
-        ++kiss;
-        ++wiss;
-      };
-      if (lane == 0)
-        for (int i = 0; i < NSW; ++i) issue_warm();
-      __syncwarp();
-
-      float2 P[CPL][8];
-      float W[CPL];  // structured: log2 decay of entry 0 over the steps walked; generic: sum of delta
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        W[c] = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) P[c][k] = make_float2(1.0f, 1.0f);
-      }
-      int np = 8;    // structured: state pairs still accumulating
-      for (int k = 0;; ++k) {
-        const int64_t thi = t0 - static_cast<int64_t>(k) * TS;
-        const int64_t tlo = thi - TS > 0 ? thi - TS : 0;
-        const int n = static_cast<int>(thi - tlo);
-        const int slot = static_cast<int>(wcon % NSW);
-        if (!mbar_wait(&r.wbar[slot], (wcon / NSW) & 1u)) { alive = false; break; }
-        const T* xs = r.wx[slot];
-        const T* ds = r.wd[slot];
-        const T* Bs = r.wB[slot];
-        if (s4d) {
-          if (np == 8) warm_s4d<8, ZOH, CPL, TS>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
-          else if (np == 4) warm_s4d<4, ZOH, CPL, TS>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
-          else if (np == 2) warm_s4d<2, ZOH, CPL, TS>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
-          else warm_s4d<1, ZOH, CPL, TS>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
-        } else {
-          warm_gen<ZOH, CPL>(xs, ds, Bs, n, lane, g, W, P, h);
-        }
-        ++wcon;
-        // Pair k holds entries 2k, 2k+1 whose log2 decay is (2k+1) W, (2k+2) W (structured). A pair is
-        // dropped once its slower entry has decayed below 2^-26 on every active channel; dropping is final.
-        float wl = -3.0e38f;
-#pragma unroll
-        for (int c = 0; c < CPL; ++c)
-          if (act[c]) wl = fmaxf(wl, s4d ? W[c] : W[c] * g[c].A2max);
-        const float wmax = warp_max(wl);
-        const bool at_start = (tlo == 0);
-        bool done;
-        if (s4d) {
-          // pair k is live while (2k+1) * wmax > kDeadLog2 (monotone in k); np shrinks to the smallest of
-          // 8, 4, 2, 1, 0 that keeps every live pair.
-          int live = 0;
-          if (wmax > kDeadLog2 / 15.0f) live = 8;
-          else if (wmax > kDeadLog2 / 13.0f) live = 7;
-          else if (wmax > kDeadLog2 / 11.0f) live = 6;
-          else if (wmax > kDeadLog2 / 9.0f) live = 5;
-          else if (wmax > kDeadLog2 / 7.0f) live = 4;
-          else if (wmax > kDeadLog2 / 5.0f) live = 3;
-          else if (wmax > kDeadLog2 / 3.0f) live = 2;
-          else if (wmax > kDeadLog2) live = 1;
-          const int want = live > 4 ? 8 : live > 2 ? 4 : live;  // 8, 4, 2, 1 or 0
-          if (want < np) np = want;
-          done = at_start || np == 0;
-        } else {
-          done = at_start || wmax <= kDeadLog2;
-        }
-        if (done) {
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            if (ZOH && s4d) {
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                h[c][q] = __fmul2_rn(h[c][q], make_float2(1.0f / static_cast<float>(2 * q + 1),
-                                                          1.0f / static_cast<float>(2 * q + 2)));
-            }
-            if (at_start && h0row[c]) {
-              // plus (decay over [0, t0)) * h0 for the entries still live (dropped ones decayed below 2^-26)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float4 v = reinterpret_cast<const float4*>(h0row[c])[q];
-                if (!s4d || 2 * q < np) h[c][2 * q] = __ffma2_rn(P[c][2 * q], make_float2(v.x, v.y), h[c][2 * q]);
-                if (!s4d || 2 * q + 1 < np)
-                  h[c][2 * q + 1] = __ffma2_rn(P[c][2 * q + 1], make_float2(v.z, v.w), h[c][2 * q + 1]);
-              }
-            }
-          }
-          break;
-        }
-        __syncwarp();
-        if (lane == 0) issue_warm();
-      }
-      if (!alive) break;
-    }
-
-    // ---- forward over [t0, t1) ----
-    for (int64_t tb = t0; tb < t1; tb += TS) {
-      const int n = static_cast<int>((t1 - tb) < TS ? (t1 - tb) : TS);
-      const int slot = static_cast<int>(cseq % NSF);
-      if (!mbar_wait(&r.fbar[slot], (cseq / NSF) & 1u)) { alive = false; break; }
-      const T* xs = r.fx[slot];
-      const T* ds = r.fd[slot];
-      if (kConvB || kConvC) {
-#pragma unroll
-        for (int j = 0; j < TS * 16 / 32; ++j) {
-          const int i = lane + 32 * j;
-          if (kConvB) {
-            float bv = tof<T>(r.fB[slot][i]);
-            if (ZOH && s4d) bv *= 1.0f / static_cast<float>((i & 15) + 1);
-            r.Bf[i] = bv;
-          }
-          if (kConvC) r.Cf[i] = tof<T>(r.fC[slot][i]);
-        }
-        __syncwarp();
-      }
-      const float* Bs = kConvB ? r.Bf : reinterpret_cast<const float*>(r.fB[slot]);
-      const float* Cs = kConvC ? r.Cf : reinterpret_cast<const float*>(r.fC[slot]);
-      T* yp = static_cast<T*>(p.y) + (b * L + tb) * p.D + d0;  // channel c at yp + 32 c
-      if (s4d) {
-        auto one = [&](int i) {
-          float xv[CPL], dv[CPL], yv[CPL];
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            xv[c] = tof<T>(xs[i * CW + c * 32 + lane]);
-            dv[c] = tof<T>(ds[i * CW + c * 32 + lane]);
-          }
-          fwd_s4d<ZOH, CPL>(xv, dv, Bs + i * 16, Cs + i * 16, A2_0, invA0, h, yv);
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) store_y(yp + 32 * c, yv[c], act[c]);
-          yp += p.D;
-        };
-        if (n == TS) {
-#pragma unroll
-          for (int i = 0; i < TS; ++i) one(i);
-        } else {
-#pragma unroll 1
-          for (int i = 0; i < n; ++i) one(i);
-        }
-      } else {
-#pragma unroll 1
-        for (int i = 0; i < n; ++i) {
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            const float yv = fwd_gen<ZOH>(tof<T>(xs[i * CW + c * 32 + lane]), tof<T>(ds[i * CW + c * 32 + lane]),
-                                          Bs + i * 16, Cs + i * 16, g[c], h[c]);
-            store_y(yp + 32 * c, yv, act[c]);
-          }
-          yp += p.D;
-        }
-      }
-      __syncwarp();
-      ++cseq;
-      if (lane == 0) issue_fwd();
-    }
+    const bool alive = __all_sync(0xffffffffu, ok)
+                           ? run_piece<true, T, ZOH, CPL, TS, NSF, TSW, NSW>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0)
+                           : run_piece<false, T, ZOH, CPL, TS, NSF, TSW, NSW>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0);
     if (!alive) break;
-    if (t1 == L && p.final_state) {
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        if (!act[c]) continue;
-        float4* fs = reinterpret_cast<float4*>(p.final_state + (b * p.D + d0 + 32 * c) * 16);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          fs[q] = make_float4(h[c][2 * q].x, h[c][2 * q].y, h[c][2 * q + 1].x, h[c][2 * q + 1].y);
-      }
-    }
   }
 
   // No copy may still be writing this warp's shared memory when the CTA exits.
-  while (cseq < iseq) {
-    if (!mbar_wait(&r.fbar[cseq % NSF], (cseq / NSF) & 1u)) break;
-    ++cseq;
+  while (wp.cseq < iseq) {
+    if (!mbar_wait(&r.fbar[wp.cseq % NSF], (wp.cseq / NSF) & 1u)) break;
+    ++wp.cseq;
   }
-  while (wcon < wiss) {
-    if (!mbar_wait(&r.wbar[wcon % NSW], (wcon / NSW) & 1u)) break;
-    ++wcon;
+  while (wp.wcon < wp.wiss) {
+    if (!mbar_wait(&r.wbar[wp.wcon % NSW], (wp.wcon / NSW) & 1u)) break;
+    ++wp.wcon;
   }
 }
 
@@ -695,14 +781,16 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint6
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int NSW>
+template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int TSW, int NSW>
 cudaError_t launch_cfg(const FwdArgs& a) {
   constexpr int CW = 32 * CPL;
   const bool bf16 = sizeof(T) == 2;
-  CUtensorMap mx, md, mB, mC;
+  CUtensorMap mx, md, mB, mC, mxw, mdw, mBw;  // forward tiles (TS rows) and warm-up tiles (TSW rows)
   const uint64_t rows = static_cast<uint64_t>(a.batch * a.L);
   if (!make_map(&mx, a.x, bf16, a.D, rows, CW, TS) || !make_map(&md, a.delta, bf16, a.D, rows, CW, TS) ||
-      !make_map(&mB, a.B, bf16, 16, rows, 16, TS) || !make_map(&mC, a.C, bf16, 16, rows, 16, TS))
+      !make_map(&mB, a.B, bf16, 16, rows, 16, TS) || !make_map(&mC, a.C, bf16, 16, rows, 16, TS) ||
+      !make_map(&mxw, a.x, bf16, a.D, rows, CW, TSW) || !make_map(&mdw, a.delta, bf16, a.D, rows, CW, TSW) ||
+      !make_map(&mBw, a.B, bf16, 16, rows, 16, TSW))
     return cudaErrorInvalidValue;
   TmaParams p;
   p.A_log = a.A_log;
@@ -713,8 +801,8 @@ cudaError_t launch_cfg(const FwdArgs& a) {
   p.D = a.D;
   p.G = (a.D + CW - 1) / CW;
   p.total = a.batch * p.G * a.L;
-  const size_t smem = sizeof(WarpRing<T, CPL, TS, NSF, NSW>) * NW + 128;
-  auto kern = scan_fwd_tma_kernel<T, ZOH, CPL, NW, TS, NSF, NSW>;
+  const size_t smem = sizeof(WarpRing<T, CPL, TS, NSF, TSW, NSW>) * NW + 128;
+  auto kern = scan_fwd_tma_kernel<T, ZOH, CPL, NW, TS, NSF, TSW, NSW>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -732,20 +820,32 @@ cudaError_t launch_cfg(const FwdArgs& a) {
   if (nwarps < 1) nwarps = 1;
   p.nwarps = nwarps;
   const int64_t nctas = (nwarps + NW - 1) / NW;
-  kern<<<static_cast<unsigned>(nctas), NW * 32, smem, a.stream>>>(mx, md, mB, mC, p);
+  kern<<<static_cast<unsigned>(nctas), NW * 32, smem, a.stream>>>(mx, md, mB, mC, mxw, mdw, mBw, p);
   return cudaGetLastError();
 }
 
-// Kernel shape: channels per lane, warps per CTA, steps per stage, forward / warm-up ring stages.
-#if SSM_TMA_CFG == 1
-constexpr int kCPL = 1, kNW = 12, kTS = 8, kNSF = 4, kNSW = 2;
+// Kernel shapes: channels per lane, warps per CTA, forward stage steps and stages, warm-up tile steps and
+// stages. fp32 inputs: 8 warps (2 per SM sub-partition) with deeper rings; bf16 inputs (half the bytes per
+// element, so smaller rings suffice): 12 warps, whose extra latency hiding is worth 12% there.
+struct ShapeF32 { static constexpr int CPL = 2, NW = 8, TS = 8, NSF = 3, TSW = 8, NSW = 2; };
+struct ShapeBF16 { static constexpr int CPL = 2, NW = 12, TS = 8, NSF = 2, TSW = 4, NSW = 2; };
+#if SSM_TMA_CFG == 1  // experiment hooks: one shape for both input types
+struct ShapeAlt { static constexpr int CPL = 2, NW = 12, TS = 8, NSF = 2, TSW = 4, NSW = 2; };
+#define SSM_SHAPE_F32 ShapeAlt
+#define SSM_SHAPE_BF16 ShapeAlt
 #elif SSM_TMA_CFG == 2
-constexpr int kCPL = 2, kNW = 6, kTS = 8, kNSF = 4, kNSW = 3;
-#elif SSM_TMA_CFG == 3
-constexpr int kCPL = 2, kNW = 8, kTS = 4, kNSF = 5, kNSW = 3;
+struct ShapeAlt { static constexpr int CPL = 2, NW = 8, TS = 8, NSF = 3, TSW = 8, NSW = 2; };
+#define SSM_SHAPE_F32 ShapeAlt
+#define SSM_SHAPE_BF16 ShapeAlt
 #else
-constexpr int kCPL = 2, kNW = 8, kTS = 8, kNSF = 3, kNSW = 2;
+#define SSM_SHAPE_F32 ShapeF32
+#define SSM_SHAPE_BF16 ShapeBF16
 #endif
+
+template <typename T, bool ZOH, typename S>
+cudaError_t launch_shape(const FwdArgs& a) {
+  return launch_cfg<T, ZOH, S::CPL, S::NW, S::TS, S::NSF, S::TSW, S::NSW>(a);
+}
 
 }  // namespace
 
@@ -765,10 +865,9 @@ bool tma_path_ok(const FwdArgs& a) {
 
 cudaError_t launch_fwd_tma(const FwdArgs& a) {
   if (a.dtype == 1)
-    return a.disc == 1 ? launch_cfg<__nv_bfloat16, true, kCPL, kNW, kTS, kNSF, kNSW>(a)
-                       : launch_cfg<__nv_bfloat16, false, kCPL, kNW, kTS, kNSF, kNSW>(a);
-  return a.disc == 1 ? launch_cfg<float, true, kCPL, kNW, kTS, kNSF, kNSW>(a)
-                     : launch_cfg<float, false, kCPL, kNW, kTS, kNSF, kNSW>(a);
+    return a.disc == 1 ? launch_shape<__nv_bfloat16, true, SSM_SHAPE_BF16>(a)
+                       : launch_shape<__nv_bfloat16, false, SSM_SHAPE_BF16>(a);
+  return a.disc == 1 ? launch_shape<float, true, SSM_SHAPE_F32>(a) : launch_shape<float, false, SSM_SHAPE_F32>(a);
 }
 
 int read_and_clear_device_status() {
