@@ -36,6 +36,7 @@ import ssm_inputs  # noqa: E402
 METRIC = "selective-scan B·L·D elems/s; achieved HBM GB/s as fraction of B300 peak"
 FALLBACK_HBM_GBS = 6400.0
 FLUSH_BYTES = 512 << 20
+FWD_SOURCES = ("scan_fwd_tma.cu", "common.cuh", "launch.h")  # the prefill kernel's own sources
 
 
 def parse_args(argv=None):
@@ -49,6 +50,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
+                    help="override a size of the workload (batch, L or D), e.g. for a small profiling case")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other prefill workloads and the decode workload (reported under 'workloads')")
     return ap.parse_args(argv)
 
 
@@ -89,7 +94,7 @@ def ncu_traffic(kernel_prefix, workload):
         return None
     from selective_state_space_124_b300 import build as lib_build
     entry = rec.get(workload, {})
-    if entry.get("source_hash") != lib_build.source_hash() or not entry.get("kernel", "").startswith(kernel_prefix):
+    if entry.get("source_hash") != lib_build.source_hash(FWD_SOURCES) or not entry.get("kernel", "").startswith(kernel_prefix):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -208,6 +213,104 @@ class ClockSampler:
                 "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.mode}
 
 
+def _dev_tensor(torch, a, bf16):
+    if bf16:
+        return torch.from_numpy(ssm_inputs.bf16_round(a).view(np.int16).copy()).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+
+
+def measure_prefill(name, reps, flush, peak):
+    """Prefill of another workload, timed like the main one (L2 flushed before each launch, CUDA events)."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    cfg = dict(ssm_inputs.WORKLOADS[name])
+    inp = ssm_inputs.workload_inputs(name)
+    bf16 = cfg["dtype"] == "bf16"
+    d = {k: _dev_tensor(torch, inp[k], bf16) for k in ("x", "delta", "B", "C")}
+    A = torch.from_numpy(inp["A_log"].copy()).cuda()
+    b, L, D, N = cfg["batch"], cfg["L"], cfg["D"], cfg["N"]
+    y = torch.empty((b, L, D), dtype=torch.bfloat16 if bf16 else torch.float32, device="cuda")
+    fs = torch.empty((b, D, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    args = (d["x"].data_ptr(), d["delta"].data_ptr(), A.data_ptr(), d["B"].data_ptr(), d["C"].data_ptr(), 0,
+            y.data_ptr(), fs.data_ptr(), b, L, D, N, cfg["dtype"], cfg["disc"], stream.cuda_stream)
+    ms = []
+    for i in range(3 + reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        lib.ssm_scan_fwd_ptr(*args)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            ms.append(e0.elapsed_time(e1))
+    lib.check_device()
+    med = statistics.median(ms) / 1e3
+    gbs = fwd_bytes(cfg) / med / 1e9
+    return {"workload": describe(name, cfg).split(";")[0], "launch_ms_median": med * 1e3,
+            "elems_per_s": b * L * D / med, "gbs": gbs, "hbm_frac": gbs / peak, "reps": reps}
+
+
+def measure_decode(steps, flush, peak):
+    """The decode workload (batch 128, D 5120, N 16, fp32 state in HBM): `steps` consecutive ssm_scan_step
+    calls over a fixed set of 16 device-resident tokens, (a) back to back as one CUDA graph (the 42 MB
+    state stays L2-resident between steps) and (b) one step at a time with the L2 flushed before each."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    cfg = dict(ssm_inputs.WORKLOADS["decode"])
+    ds = ssm_inputs.DecodeStream(**cfg)
+    batch, D, N = cfg["batch"], cfg["D"], cfg["N"]
+    toks = [ds.next_step() for _ in range(16)]
+    dt = [{k: _dev_tensor(torch, t[k], False) for k in ("x", "delta", "B", "C")} for t in toks]
+    A = torch.from_numpy(ds.A_log.copy()).cuda()
+    state = torch.from_numpy(ds.state0.copy()).cuda()
+    y = torch.empty((batch, D), dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    def step_args(i, s):
+        t = dt[i % 16]
+        return (state.data_ptr(), t["x"].data_ptr(), t["delta"].data_ptr(), A.data_ptr(), t["B"].data_ptr(),
+                t["C"].data_ptr(), y.data_ptr(), batch, D, N, "f32", cfg["disc"], s.cuda_stream)
+    per_graph = 100
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for i in range(3):
+            lib.ssm_scan_step_ptr(*step_args(i, side))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(per_graph):
+                lib.ssm_scan_step_ptr(*step_args(i, side))
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // per_graph)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    resident = e0.elapsed_time(e1) / 1e3 / (reps * per_graph)
+    stream = torch.cuda.current_stream()
+    ms = []
+    for i in range(3 + 50):
+        flush.zero_()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        lib.ssm_scan_step_ptr(*step_args(i, stream))
+        a1.record(stream)
+        if i >= 3:
+            ms.append((a0, a1))
+    torch.cuda.synchronize()
+    lib.check_device()
+    cold = statistics.median(a.elapsed_time(b_) for a, b_ in ms) / 1e3
+    nb = step_bytes(cfg)
+    return {"workload": f"decode: batch {batch}, D {D}, N {N}, fp32 state, {cfg['disc']}",
+            "steps_timed": reps * per_graph, "us_per_step_l2_resident": resident * 1e6,
+            "state_entries_per_s_l2_resident": batch * D * N / resident,
+            "us_per_step_l2_flushed": cold * 1e6, "gbs_l2_flushed": nb / cold / 1e9,
+            "hbm_frac_l2_flushed": nb / cold / 1e9 / peak, "bytes_per_step": nb}
+
+
 def dist_setup():
     return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -300,8 +403,14 @@ def main(argv=None):
     if world > 1:
         dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
 
-    cfg = dict(ssm_inputs.WORKLOADS[args.workload])
-    inp = ssm_inputs.workload_inputs(args.workload, seed=rank_seed(rank))
+    overrides = {}
+    for kv in args.set:
+        k, v = kv.split("=", 1)
+        if k not in ("batch", "L", "D"):
+            raise SystemExit(f"--set: unknown size {k!r} (batch, L or D)")
+        overrides[k] = int(v)
+    cfg = dict(ssm_inputs.WORKLOADS[args.workload], **overrides)
+    inp = ssm_inputs.workload_inputs(args.workload, seed=rank_seed(rank), **overrides)
     tok = ssm_inputs.token_inputs(cfg["batch"], cfg["D"], cfg["N"], seed=1000 + rank_seed(rank),
                                   mu=cfg["mu"], sigma=cfg["sigma"])
     bf16 = cfg["dtype"] == "bf16"
@@ -429,6 +538,13 @@ def main(argv=None):
         "e2e": e2e,
         "gpu_launches": 2 * K,
     }
+    if not args.no_extra and world == 1:
+        extra = {}
+        for name in ("long", "mamba1p4b"):
+            if name != args.workload:
+                extra[name] = measure_prefill(name, 10, flush, peak)
+        extra["decode"] = measure_decode(1000, flush, peak)
+        line["workloads"] = extra
     if not args.no_cpu_baseline:
         r, cores, sample = cpu_oracle_rate(inp, cfg, oracle_sample(inp, cfg, args.cpu_seconds))
         line["cpu_baseline"] = {"value": r, "unit": "elems/s", "cores": cores, "kind": "oracle", "sample": sample}

@@ -29,11 +29,14 @@ def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def source_hash() -> str:
-    """Hash of the kernel sources and the header (identifies the kernels a profile was taken on)."""
+def source_hash(files=None) -> str:
+    """Hash of kernel sources (identifies the code a profile was taken on): the given csrc file names, or
+    every csrc file and the header."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INCLUDE, "*.h"))):
+    paths = [os.path.join(CSRC, f) for f in files] if files else \
+        glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    for f in sorted(paths):
         if os.path.isfile(f):
             h.update(os.path.basename(f).encode())
             with open(f, "rb") as fh:

@@ -479,11 +479,13 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
       const int64_t tlo = thi - TSW > 0 ? thi - TSW : 0;
       const int slot = static_cast<int>(wp.wiss % NSW);
       const int trow = static_cast<int>(b * L + tlo);
-      mbar_arrive_tx(&r.wbar[slot], kWarmBytes);
-      tma_load(r.wx[slot], mx, col, trow, &r.wbar[slot]);
-      tma_load(r.wd[slot], md, col, trow, &r.wbar[slot]);
-      tma_load(r.wB[slot], mB, 0, trow, &r.wbar[slot]);
-      ++kiss;
+      if (lane == 0) {
+        mbar_arrive_tx(&r.wbar[slot], kWarmBytes);
+        tma_load(r.wx[slot], mx, col, trow, &r.wbar[slot]);
+        tma_load(r.wd[slot], md, col, trow, &r.wbar[slot]);
+        tma_load(r.wB[slot], mB, 0, trow, &r.wbar[slot]);
+      }
+      ++kiss;  // every lane keeps the counters (warp-uniform)
       ++wp.wiss;
     };
 
@@ -564,7 +566,7 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
         break;
       }
       __syncwarp();
-      if (lane == 0) issue_warm();
+      issue_warm();
     }
   }
 
@@ -627,7 +629,7 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
     }
     __syncwarp();
     ++wp.cseq;
-    if (lane == 0) issue_fwd();
+    issue_fwd();
   }
   if (t1 == L && p.final_state) {
 #pragma unroll
@@ -659,6 +661,11 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * NW + warp;
   if (wid >= p.nwarps) return;
 
+  if (threadIdx.x == 0) {  // bring the copy descriptors into the descriptor cache before their first use
+    const CUtensorMap* maps[7] = {&mx, &md, &mB, &mC, &mxw, &mdw, &mBw};
+#pragma unroll
+    for (int i = 0; i < 7; ++i) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(maps[i])) : "memory");
+  }
   if (lane == 0) {
     for (int i = 0; i < NSF; ++i) mbar_init(&r.fbar[i], 1);
     for (int i = 0; i < NSW; ++i) mbar_init(&r.wbar[i], 1);
@@ -672,8 +679,9 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
   const int64_t L = p.L;
 
   // Forward stages, in the order the consumer takes them: the range [lo0, hi0) cut at row ends and every
-  // TS steps. Lane 0 issues them NSF ahead of consumption. The cursor advances without divisions (64-bit
-  // division is a long software sequence).
+  // TS steps, issued NSF ahead of consumption. Every lane advances the cursor and the counters (so that they
+  // stay warp-uniform for the warp-wide waits); lane 0 issues the copies. The cursor advances without
+  // divisions (64-bit division is a long software sequence).
   int64_t ipos = lo0;   // first step of the next forward stage to issue
   uint32_t iseq = 0;    // forward stages issued
   int64_t it = lo0 % L, ib = (lo0 / L) / p.G, ig = (lo0 / L) % p.G;  // its step, batch, channel group
@@ -684,11 +692,13 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
     const int slot = static_cast<int>(iseq % NSF);
     const int trow = static_cast<int>(ib * L + it);
     const int col = static_cast<int>(ig * CW);
-    mbar_arrive_tx(&r.fbar[slot], kFwdBytes);
-    tma_load(r.fx[slot], &mx, col, trow, &r.fbar[slot]);
-    tma_load(r.fd[slot], &md, col, trow, &r.fbar[slot]);
-    tma_load(r.fB[slot], &mB, 0, trow, &r.fbar[slot]);
-    tma_load(r.fC[slot], &mC, 0, trow, &r.fbar[slot]);
+    if (lane == 0) {
+      mbar_arrive_tx(&r.fbar[slot], kFwdBytes);
+      tma_load(r.fx[slot], &mx, col, trow, &r.fbar[slot]);
+      tma_load(r.fd[slot], &md, col, trow, &r.fbar[slot]);
+      tma_load(r.fB[slot], &mB, 0, trow, &r.fbar[slot]);
+      tma_load(r.fC[slot], &mC, 0, trow, &r.fbar[slot]);
+    }
     ipos += n;
     it += n;
     if (it == L) {
@@ -700,32 +710,49 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
     }
     ++iseq;
   };
-  if (lane == 0)
-    for (int i = 0; i < NSF; ++i) issue_fwd();
-
   WarpPipe wp{0u, 0u, 0u};
+  bool primed = false;
   int64_t lo = lo0;
   while (lo < hi0) {
     const int64_t row = lo / L, t0 = lo % L;
     const int64_t t1 = (hi0 - lo < L - t0) ? t0 + (hi0 - lo) : L;
     lo += t1 - t0;
-    int kiss0 = 0;
-    if (t0 > 0) {
-      kiss0 = warm_prologue(r, &mxw, &mdw, &mBw, lane, (row / p.G) * L, static_cast<int>((row % p.G) * CW), t0, wp);
-      if (kiss0 < 0) break;
-    }
-    // S4D structure check (warp-uniform): A[d, n] = (n + 1) A[d, 0] for every channel of the warp.
+    // This piece's A_log rows are loaded into registers before any bulk copy is issued, so that these small
+    // loads enter the memory system ahead of the warps' first tiles (behind them they wait microseconds).
     const int64_t d0 = (row % p.G) * CW + lane;
-    bool ok = true;
+    float Alog[CPL][16];
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
       const int64_t d = d0 + 32 * c;
-      if (d < p.D) {
-        const float A0 = -expf(__ldg(p.A_log + d * 16));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = d < p.D ? __ldg(reinterpret_cast<const float4*>(p.A_log + d * 16) + q)
+                                 : make_float4(0.0f, 0.6931472f, 1.0986123f, 1.3862944f);
+        Alog[c][4 * q] = v.x;
+        Alog[c][4 * q + 1] = v.y;
+        Alog[c][4 * q + 2] = v.z;
+        Alog[c][4 * q + 3] = v.w;
+      }
+    }
+    int kiss0 = 0;
+    if (t0 > 0) {  // the walk's first tiles go out before the forward ring is primed: they are needed first
+      kiss0 = warm_prologue(r, &mxw, &mdw, &mBw, lane, (row / p.G) * L, static_cast<int>((row % p.G) * CW), t0, wp);
+      if (kiss0 < 0) break;
+    }
+    if (!primed) {
+      for (int i = 0; i < NSF; ++i) issue_fwd();
+      primed = true;
+    }
+    // S4D structure check (warp-uniform): A[d, n] = (n + 1) A[d, 0] for every channel of the warp.
+    bool ok = true;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      if (d0 + 32 * c < p.D) {
+        const float A0 = -expf(Alog[c][0]);
         bool okc = A0 < -1e-30f && A0 > -3.0e38f;
 #pragma unroll
         for (int n = 1; n < 16; ++n) {
-          const float A = -expf(__ldg(p.A_log + d * 16 + n));
+          const float A = -expf(Alog[c][n]);
           okc = okc && fabsf(A - static_cast<float>(n + 1) * A0) <= 4.8e-7f * fabsf(A);
         }
         ok = ok && okc;
@@ -858,6 +885,7 @@ bool tma_path_ok(const FwdArgs& a) {
     if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return false;
   if (a.final_state && reinterpret_cast<uintptr_t>(a.final_state) % 16 != 0) return false;
   if (a.h0 && reinterpret_cast<uintptr_t>(a.h0) % 16 != 0) return false;
+  if (reinterpret_cast<uintptr_t>(a.A_log) % 16 != 0) return false;  // rows read as float4
   if (a.batch * a.L > (int64_t(1) << 30)) return false;  // TMA row coordinates are 32-bit
   if (encoder() == nullptr) return false;
   return true;

@@ -1,7 +1,12 @@
 // scan_step.cu -- one recurrent decode step ("Understanding Mamba" s3.2 / s10.1): for every (b, d) the
 // N-entry state is read, advanced by Eq. (3) with this token's delta, B, C, written back in place, and
-// y_t = C_t . h_t is produced. One thread per channel; the state row (N floats) is contiguous, so a warp
-// reads and writes 32 consecutive rows.
+// y_t = C_t . h_t is produced.
+//
+// N = 16 with 16-byte-aligned rows (the common case): four lanes per channel, each owning four state
+// entries, so every load and store of state, A_log, B and C is one coalesced 16-byte access per lane (a warp
+// moves 512 contiguous bytes of state per instruction). The read-out sums the four lanes' partial dot products
+// with two shuffles. A persistent grid walks the (batch, channel) quads. Other shapes: one thread per
+// channel.
 #include "common.cuh"
 #include "launch.h"
 
@@ -18,6 +23,99 @@ struct StepParams {
   void* y;
   int64_t batch, D, N;
 };
+
+// ---- N = 16: four lanes per channel ---------------------------------------------------------------------
+template <typename T> struct Vec4;
+template <> struct Vec4<float> {
+  __device__ __forceinline__ static float4 load(const void* p, int64_t i) {  // elements i .. i+3
+    return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p) + i));
+  }
+};
+template <> struct Vec4<__nv_bfloat16> {
+  __device__ __forceinline__ static float4 load(const void* p, int64_t i) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p) + i));
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xffff0000u));
+  }
+};
+
+// One state entry: dl = delta * log2(e), u = delta * x (Euler) or x (ZOH).
+template <bool ZOH>
+__device__ __forceinline__ float step_entry(float& h, float alog, float dl, float dt, float u, float bn, float cn) {
+  const float a2 = alog * kLog2e;
+  const float ea = ex2(a2);             // exp(A_log) = -A
+  const float w = -ea * dl;             // delta * A * log2(e)
+  const float e = exp2m1(w, ex2(w));    // Abar - 1
+  float bx;
+  if (ZOH) {  // (Abar - 1) / A = -e / exp(A_log); where A is 0 in fp32, its limit delta
+    const float coef = ea == 0.0f ? dt : -e * ex2(-a2);
+    bx = coef * bn * u;
+  } else {
+    bx = u * bn;
+  }
+  h = fmaf(e, h, h) + bx;
+  return cn * h;
+}
+
+struct QuadIn {  // one lane's share of a channel: four state entries and their inputs
+  float4 h, al, bb, cc;
+  float xv, dt;
+};
+
+template <typename T>
+__device__ __forceinline__ void quad_load(const StepParams& p, int64_t ch, int q, QuadIn& v) {
+  // batch * D < 2^31 is checked on the host: a 32-bit division is a short sequence, a 64-bit one is not
+  const uint32_t b32 = static_cast<uint32_t>(ch) / static_cast<uint32_t>(p.D);
+  const int64_t b = b32, d = ch - b * p.D;
+  v.h = reinterpret_cast<const float4*>(p.state + ch * 16)[q];
+  v.al = __ldg(reinterpret_cast<const float4*>(p.A_log + d * 16) + q);
+  v.bb = Vec4<T>::load(p.B, b * 16 + 4 * q);
+  v.cc = Vec4<T>::load(p.C, b * 16 + 4 * q);
+  v.xv = Elem<T>::load(p.x, ch);
+  v.dt = Elem<T>::load(p.delta, ch);
+}
+
+template <bool ZOH>
+__device__ __forceinline__ float quad_step(QuadIn& v) {
+  const float dl = v.dt * kLog2e, u = ZOH ? v.xv : v.dt * v.xv;
+  float yv = step_entry<ZOH>(v.h.x, v.al.x, dl, v.dt, u, v.bb.x, v.cc.x);
+  yv += step_entry<ZOH>(v.h.y, v.al.y, dl, v.dt, u, v.bb.y, v.cc.y);
+  yv += step_entry<ZOH>(v.h.z, v.al.z, dl, v.dt, u, v.bb.z, v.cc.z);
+  yv += step_entry<ZOH>(v.h.w, v.al.w, dl, v.dt, u, v.bb.w, v.cc.w);
+  return yv;
+}
+
+// Persistent grid over the (channel, quad) items; each trip handles two items, both loaded before either is
+// computed, so that every lane keeps two state rows' worth of loads in flight.
+template <bool ZOH, typename T>
+__global__ void __launch_bounds__(256) scan_step_quad_kernel(StepParams p, int64_t quads) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t span = 2 * stride;
+  const int64_t bound = quads + (span - quads % span) % span;  // same trip count for every lane of a warp
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < bound; i0 += span) {
+    const int64_t i1 = i0 + stride;
+    const bool live0 = i0 < quads, live1 = i1 < quads;
+    const int q = static_cast<int>(i0 & 3);  // stride is a multiple of 4: both items use entries 4q .. 4q+3
+    QuadIn v0, v1;
+    if (live0) quad_load<T>(p, i0 >> 2, q, v0);
+    if (live1) quad_load<T>(p, i1 >> 2, q, v1);
+    float y0 = 0.0f, y1 = 0.0f;
+    if (live0) {
+      y0 = quad_step<ZOH>(v0);
+      reinterpret_cast<float4*>(p.state + (i0 >> 2) * 16)[q] = v0.h;
+    }
+    if (live1) {
+      y1 = quad_step<ZOH>(v1);
+      reinterpret_cast<float4*>(p.state + (i1 >> 2) * 16)[q] = v1.h;
+    }
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (live0 && q == 0) Elem<T>::store(p.y, i0 >> 2, y0);
+    if (live1 && q == 0) Elem<T>::store(p.y, i1 >> 2, y1);
+  }
+}
 
 template <int NP, bool ZOH, typename T, bool VEC>
 __global__ void __launch_bounds__(256) scan_step_kernel(StepParams p) {
@@ -79,6 +177,17 @@ cudaError_t go(const StepParams& sp, cudaStream_t s) {
 template <bool ZOH, typename T>
 cudaError_t pick(const StepParams& sp, cudaStream_t s) {
   const bool aligned = (reinterpret_cast<uintptr_t>(sp.state) & 15) == 0;
+  const uintptr_t bc_align = sizeof(T) == 2 ? 7 : 15;
+  if (sp.N == 16 && aligned && sp.batch * sp.D < (int64_t(1) << 31) && (reinterpret_cast<uintptr_t>(sp.A_log) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(sp.B) & bc_align) == 0 && (reinterpret_cast<uintptr_t>(sp.C) & bc_align) == 0) {
+    const int64_t quads = sp.batch * sp.D * 4;
+    int64_t blocks = (quads + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 8;  // persistent: 8 resident 256-thread blocks per SM
+    blocks = (blocks + 1) / 2;                                   // two items per lane per trip
+    if (blocks > cap) blocks = cap;
+    scan_step_quad_kernel<ZOH, T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(sp, quads);
+    return cudaGetLastError();
+  }
   if (sp.N == 16 && aligned) return go<16, ZOH, T, true>(sp, s);
   if (sp.N == 8 && aligned) return go<8, ZOH, T, true>(sp, s);
   if (sp.N == 4 && aligned) return go<4, ZOH, T, true>(sp, s);
