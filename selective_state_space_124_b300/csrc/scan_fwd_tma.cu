@@ -304,20 +304,26 @@ __device__ __forceinline__ void warm_gen(const T* xs, const T* ds, const T* Bs, 
 }
 
 // ---- one forward step (structured A) for the CPL channels of a lane, from fp32 B / C rows in shared memory -
+// Split in two: the per-step decay factors e and input scalar s depend only on x and delta (fwd_prep), the
+// recurrence and read-out (fwd_core) on the carried state. A stage computes step i+1's fwd_prep before step
+// i's fwd_core, so the scheduler always has the next step's independent decay tree to interleave with the
+// current step's dependent update chain.
 template <bool ZOH, int CPL>
-__device__ __forceinline__ void fwd_s4d(const float (&xv)[CPL], const float (&dv)[CPL], const float* Brow,
-                                        const float* Crow, const float (&A2_0)[CPL], const float (&invA0)[CPL],
-                                        float2 (&h)[CPL][8], float (&y)[CPL]) {
-  const float4* Bq = reinterpret_cast<const float4*>(Brow);
-  const float4* Cq = reinterpret_cast<const float4*>(Crow);
-  float2 e[CPL][8];
-  float2 s[CPL];  // per channel: x / A_0 (ZOH) or delta * x (Euler)
+__device__ __forceinline__ void fwd_prep(const float (&xv)[CPL], const float (&dv)[CPL], const float (&A2_0)[CPL],
+                                         const float (&invA0)[CPL], float2 (&e)[CPL][8], float2 (&s)[CPL]) {
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) {
+  for (int c = 0; c < CPL; ++c) {  // s: x / A_0 (ZOH) or delta * x (Euler)
     const float w = dv[c] * A2_0[c];
     em1_tree<8>(exp2m1(w, ex2(w)), e[c]);
     s[c] = bc2(ZOH ? xv[c] * invA0[c] : dv[c] * xv[c]);
   }
+}
+
+template <bool ZOH, int CPL>
+__device__ __forceinline__ void fwd_core(const float2 (&e)[CPL][8], const float2 (&s)[CPL], const float* Brow,
+                                         const float* Crow, float2 (&h)[CPL][8], float (&y)[CPL]) {
+  const float4* Bq = reinterpret_cast<const float4*>(Brow);
+  const float4* Cq = reinterpret_cast<const float4*>(Crow);
   float2 ya[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) ya[c] = make_float2(0.0f, 0.0f);
@@ -347,6 +353,16 @@ __device__ __forceinline__ void fwd_s4d(const float (&xv)[CPL], const float (&dv
   }
 #pragma unroll
   for (int c = 0; c < CPL; ++c) y[c] = ya[c].x + ya[c].y;
+}
+
+template <bool ZOH, int CPL>
+__device__ __forceinline__ void fwd_s4d(const float (&xv)[CPL], const float (&dv)[CPL], const float* Brow,
+                                        const float* Crow, const float (&A2_0)[CPL], const float (&invA0)[CPL],
+                                        float2 (&h)[CPL][8], float (&y)[CPL]) {
+  float2 e[CPL][8];
+  float2 s[CPL];
+  fwd_prep<ZOH, CPL>(xv, dv, A2_0, invA0, e, s);
+  fwd_core<ZOH, CPL>(e, s, Brow, Crow, h, y);
 }
 
 template <bool ZOH>
@@ -605,7 +621,41 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
         }
         yp += p.D;
       };
-      if (n == TS && full) {
+      // fp32 inputs (8-warp shape, registers to spare): step i+1's decay tree is computed before step i's
+      // update, 8% faster on the long ZOH workload. bf16 inputs run 12 warps capped at 168 registers, where
+      // the extra live values cost more than they gain.
+      constexpr bool kPipe = sizeof(T) == 4;
+      if (kPipe && n == TS && full) {
+        float2 e[CPL][8], s2[CPL];
+        auto prep = [&](int i, float2 (&ee)[CPL][8], float2 (&ss)[CPL]) {
+          float xv[CPL], dv[CPL];
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            xv[c] = tof<T>(xs[i * CW + c * 32 + lane]);
+            dv[c] = tof<T>(ds[i * CW + c * 32 + lane]);
+          }
+          fwd_prep<ZOH, CPL>(xv, dv, A2_0, invA0, ee, ss);
+        };
+        prep(0, e, s2);
+#pragma unroll
+        for (int i = 0; i < TS; ++i) {
+          float2 en[CPL][8], sn[CPL];
+          if (i + 1 < TS) prep(i + 1, en, sn);
+          float yv[CPL];
+          fwd_core<ZOH, CPL>(e, s2, Bs + i * 16, Cs + i * 16, h, yv);
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) store_y(yp + 32 * c, yv[c]);
+          yp += p.D;
+          if (i + 1 < TS) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+              s2[c] = sn[c];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) e[c][k] = en[c][k];
+            }
+          }
+        }
+      } else if (n == TS && full) {
 #pragma unroll
         for (int i = 0; i < TS; ++i) one(std::true_type{}, i);
       } else if (n == TS) {
