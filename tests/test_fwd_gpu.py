@@ -259,3 +259,33 @@ def test_fwd_generic_A_long_walks(orc, disc, D):
     check_fwd(orc, inp, "f32", disc)
     inp["delta"] = np.random.default_rng(33).uniform(-1e-4, 1e-4, inp["delta"].shape).astype(np.float32)
     check_fwd(orc, inp, "f32", disc)
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_fwd_tma_short_ranges_cross_rows(orc, disc):
+    """Many short per-warp ranges (32 steps): most start mid-row and rebuild their carry by a warm-up walk
+    longer than the range itself, several reach t = 0 and add the decayed h0, and ranges cross row ends
+    into the next (batch, channel-group) row."""
+    batch, L, D, N = 3, 700, 192, 16
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=41)
+    h0 = np.random.default_rng(42).standard_normal((batch, D, N)).astype(np.float32)
+    check_fwd(orc, inp, "f32", disc, h0=h0)
+
+
+def test_fwd_misaligned_A_log_uses_general_path(orc):
+    """A_log that is not 16-byte aligned cannot be read as float4 rows: the general kernel runs instead."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    from gpu_util import dev_inputs
+    batch, L, D, N = 2, 400, 128, 16
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=43)
+    d = dev_inputs(inp, "f32")
+    flat = torch.zeros(D * N + 1, device="cuda")
+    flat[1:] = d["A_log"].reshape(-1)
+    A_off = flat[1:].view(D, N)  # 4 bytes past a 16-byte boundary
+    assert A_off.data_ptr() % 16 == 4
+    y, fs = lib.ssm_scan_fwd(d["x"], d["delta"], A_off, d["B"], d["C"], disc="zoh")
+    lib.check_device()
+    yr, sr = orc.scan_fwd(inp["x"], inp["delta"], inp["A_log"], inp["B"], inp["C"], disc="zoh")
+    assert rel_err(y.cpu().numpy(), yr) <= TOL["f32"]
+    assert rel_err(fs.cpu().numpy(), sr) <= TOL["f32"]

@@ -60,3 +60,9 @@ def test_reference_arm_line(capsys):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "elems/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_bench_size_overrides_parse():
+    import bench
+    a = bench.parse_args(["--workload", "long", "--set", "L=16384", "--set", "batch=2", "--no-extra"])
+    assert a.workload == "long" and a.set == ["L=16384", "batch=2"] and a.no_extra

@@ -92,3 +92,28 @@ def test_workload_decode_1000_steps(orc):
         assert ey <= TOL["f32"], f"step {step}: y rel err {ey:.3g}"
         assert es <= TOL["f32"], f"step {step}: state rel err {es:.3g}"
     lib.check_device()
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_step_misaligned_A_log_and_many_quads(orc, disc):
+    """The four-lanes-per-channel kernel over more (channel, quad) items than one grid pass holds, and the
+    one-thread-per-channel kernel when A_log is not 16-byte aligned; both against the oracle."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    batch, D, N = 40, 3000, 16   # 480k quads: several trips of the persistent grid, ragged last trip
+    rng = np.random.default_rng(51)
+    st = rng.standard_normal((batch, D, N)).astype(np.float32)
+    x = rng.standard_normal((batch, D)).astype(np.float32)
+    dt = np.log1p(np.exp(rng.normal(-2, 1, (batch, D)))).astype(np.float32)
+    B = rng.standard_normal((batch, N)).astype(np.float32)
+    C = rng.standard_normal((batch, N)).astype(np.float32)
+    A_log = ssm_inputs.a_log_s4d(D, N)
+    sr, yr = orc.scan_step(st.astype(np.float64), x, dt, A_log, B, C, disc=disc)
+    flat = torch.zeros(D * N + 1, device="cuda")
+    flat[1:] = torch.from_numpy(A_log).cuda().reshape(-1)
+    for A_dev in (torch.from_numpy(A_log).cuda(), flat[1:].view(D, N)):
+        state = torch.from_numpy(st).cuda()
+        y = lib.ssm_scan_step(state, _dev(x, "f32"), _dev(dt, "f32"), A_dev, _dev(B, "f32"), _dev(C, "f32"), disc=disc)
+        lib.check_device()
+        assert rel_err(y.cpu().numpy(), yr) <= TOL["f32"]
+        assert rel_err(state.cpu().numpy(), sr) <= TOL["f32"]
