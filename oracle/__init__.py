@@ -62,6 +62,12 @@ class Oracle:
         lib.oracle_scan_fwd.restype = i32
         lib.oracle_scan_step.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, vp, i64, vp]
         lib.oracle_scan_step.restype = i32
+        lib.oracle_scan_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i64, i64, i64, i64, i32, i32,
+                                           vp, i64, vp, vp]
+        lib.oracle_scan_fwd_ex.restype = i32
+        lib.oracle_scan_step_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i64, i64, i64, i32, i32, vp,
+                                            i64, vp]
+        lib.oracle_scan_step_ex.restype = i32
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         self.lib = lib
@@ -69,18 +75,26 @@ class Oracle:
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
 
-    def scan_fwd(self, x, delta, A_log, B, C, disc="euler", h0=None, channels=None, f64=None):
+    def scan_fwd(self, x, delta, A_log, B, C, disc="euler", h0=None, channels=None, f64=None,
+                 delta_bias=None, delta_softplus=False, D_skip=None, z=None):
         """Prefill scan. x, delta: [batch, L, D]; B, C: [batch, L, N]; A_log: [D, N].
 
         Returns (y, final_state) in float64. With ``channels`` None: y [batch, L, D] and
         final_state [batch, D, N]; otherwise (a list of flat channel ids b*D + d) y [n_chan, L] and
         final_state [n_chan, N]. ``h0`` (optional) is indexed like final_state. Inputs are passed as
         float32 unless any of them is float64 (or ``f64`` is set), in which case all go as float64.
+
+        Optional layer pieces (see ssm_oracle.c): delta = softplus(delta + delta_bias[d]) when
+        ``delta_softplus`` (bias [D], default 0), y = (y + D_skip[d] x) * SiLU(z) with D_skip [D] and
+        z [batch, L, D] each optional.
         """
-        arrs = [np.asarray(a) for a in (x, delta, A_log, B, C)]
+        arrs = [np.asarray(a) for a in (x, delta, A_log, B, C)] + ([np.asarray(z)] if z is not None else [])
         if f64 is None:
             f64 = any(a.dtype == np.float64 for a in arrs)
-        x, delta, A_log, B, C = (_as_input(a, f64) for a in arrs)
+        x, delta, A_log, B, C = (_as_input(a, f64) for a in arrs[:5])
+        zc = None if z is None else _as_input(z, f64)
+        bias = None if delta_bias is None else np.ascontiguousarray(delta_bias, np.float64)
+        dsk = None if D_skip is None else np.ascontiguousarray(D_skip, np.float64)
         batch, L, D = x.shape
         N = A_log.shape[1]
         assert delta.shape == x.shape and A_log.shape == (D, N)
@@ -92,9 +106,15 @@ class Oracle:
         h0c = None
         if h0 is not None:
             h0c = np.ascontiguousarray(np.asarray(h0, np.float64).reshape(n_chan, N))
-        rc = self.lib.oracle_scan_fwd(
+        assert zc is None or zc.shape == x.shape
+        assert bias is None or bias.shape == (D,)
+        assert dsk is None or dsk.shape == (D,)
+        rc = self.lib.oracle_scan_fwd_ex(
             x.ctypes.data, delta.ctypes.data, A_log.ctypes.data, B.ctypes.data, C.ctypes.data,
-            None if h0c is None else h0c.ctypes.data, batch, L, D, N, DISC[disc], int(f64),
+            None if h0c is None else h0c.ctypes.data,
+            None if bias is None else bias.ctypes.data, int(bool(delta_softplus)),
+            None if dsk is None else dsk.ctypes.data, None if zc is None else zc.ctypes.data,
+            batch, L, D, N, DISC[disc], int(f64),
             None if chan is None else chan.ctypes.data, n_chan, y.ctypes.data, st.ctypes.data)
         if rc != 0:
             raise ValueError("oracle_scan_fwd rejected its arguments")
@@ -102,13 +122,18 @@ class Oracle:
             return y.reshape(batch, D, L).transpose(0, 2, 1).copy(), st.reshape(batch, D, N)
         return y, st
 
-    def scan_step(self, state, x_t, delta_t, A_log, B_t, C_t, disc="euler", channels=None, f64=None):
+    def scan_step(self, state, x_t, delta_t, A_log, B_t, C_t, disc="euler", channels=None, f64=None,
+                  delta_bias=None, delta_softplus=False, D_skip=None, z_t=None):
         """One decode step. state: [batch, D, N] (or [n_chan, N] with ``channels``) float64;
-        x_t, delta_t: [batch, D]; B_t, C_t: [batch, N]. Returns (new_state, y_t)."""
-        arrs = [np.asarray(a) for a in (x_t, delta_t, A_log, B_t, C_t)]
+        x_t, delta_t: [batch, D]; B_t, C_t: [batch, N]. Returns (new_state, y_t). The optional layer
+        pieces are those of ``scan_fwd`` (z_t [batch, D])."""
+        arrs = [np.asarray(a) for a in (x_t, delta_t, A_log, B_t, C_t)] + ([np.asarray(z_t)] if z_t is not None else [])
         if f64 is None:
             f64 = any(a.dtype == np.float64 for a in arrs)
-        x_t, delta_t, A_log, B_t, C_t = (_as_input(a, f64) for a in arrs)
+        x_t, delta_t, A_log, B_t, C_t = (_as_input(a, f64) for a in arrs[:5])
+        zc = None if z_t is None else _as_input(z_t, f64)
+        bias = None if delta_bias is None else np.ascontiguousarray(delta_bias, np.float64)
+        dsk = None if D_skip is None else np.ascontiguousarray(D_skip, np.float64)
         batch, D = x_t.shape
         N = A_log.shape[1]
         chan = None if channels is None else np.ascontiguousarray(channels, dtype=np.int64)
@@ -116,9 +141,11 @@ class Oracle:
         st = np.array(state, dtype=np.float64, copy=True).reshape(n_chan, N)
         st = np.ascontiguousarray(st)
         y = np.empty(n_chan, np.float64)
-        rc = self.lib.oracle_scan_step(
+        rc = self.lib.oracle_scan_step_ex(
             st.ctypes.data, x_t.ctypes.data, delta_t.ctypes.data, A_log.ctypes.data, B_t.ctypes.data,
-            C_t.ctypes.data, batch, D, N, DISC[disc], int(f64),
+            C_t.ctypes.data, None if bias is None else bias.ctypes.data, int(bool(delta_softplus)),
+            None if dsk is None else dsk.ctypes.data, None if zc is None else zc.ctypes.data,
+            batch, D, N, DISC[disc], int(f64),
             None if chan is None else chan.ctypes.data, n_chan, y.ctypes.data)
         if rc != 0:
             raise ValueError("oracle_scan_step rejected its arguments")

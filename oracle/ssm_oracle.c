@@ -26,6 +26,13 @@
  *   h starts at 0 (or at h0 when given)             "Understanding Mamba" s3.1 (h_{-1} = 0)
  *   final_state[b,d,:] = h after the last step      aiwiki reference loop keeps a [B, D, N] state
  *
+ * The _ex entry points add the layer pieces around the scan that the pages define next to it:
+ *   delta  = softplus(delta_raw + bias[d])          "Understanding Mamba" s5.1, Eq. (6) (softplus of the
+ *            (when asked; softplus(v) = ln(1+e^v))    projection plus its bias b_Delta)
+ *   y_out  = (sum_n C h + Dskip[d] * x) * SiLU(z)   Eq. (1)/(3) feedthrough D x, "one independent, final
+ *            SiLU(v) = v * sigma(v)                  + D * x_t" (s2.1); the gate y (.) SiLU(z) of Eq. (9)
+ *                                                    (s8.1); each piece optional (bias 0, Dskip 0, no z)
+ *
  * Layouts (all row-major, dense): x, delta: [batch, L, D]; B, C: [batch, L, N]; A_log: [D, N];
  * h0 / final_state: [batch, D, N] (or [n_chan, N] with a channel list, see below).
  * Inputs arrive as float (fp32 values, or bf16 values widened exactly to fp32 by the caller) or,
@@ -64,6 +71,27 @@ static double oracle_bbar_x(double dlt, double a_n, double b_n, double x, int di
     return dlt * b_n * x;
 }
 
+/* delta as the recurrence uses it: the given value, or softplus(raw + bias[d]) computed as
+   max(v, 0) + log1p(exp(-|v|)) (the same function, without overflow for large v). */
+static double oracle_delta(double raw, const double *bias, int64_t d, int softplus)
+{
+    double v = raw + (bias ? bias[d] : 0.0);
+    if (!softplus) return v;
+    return (v > 0.0 ? v : 0.0) + log1p(exp(-fabs(v)));
+}
+
+/* The output of one channel at one step: read-out plus feedthrough, times the SiLU gate when z is given. */
+static double oracle_output(double yssm, double x, const double *dskip, int64_t d, const void *z, int64_t zi,
+                            int is_f64)
+{
+    double out = yssm + (dskip ? dskip[d] * x : 0.0);
+    if (z) {
+        double zv = ld(z, zi, is_f64);
+        out *= zv / (1.0 + exp(-zv));
+    }
+    return out;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP
@@ -77,11 +105,12 @@ int oracle_num_threads(void)
  * Prefill scan over whole sequences. Returns 0 on success, -1 on a bad argument.
  * h0 may be NULL (zero initial state); when given it is indexed like state_out (per listed channel).
  */
-int oracle_scan_fwd(const void *x, const void *delta, const void *A_log,
-                    const void *B, const void *C, const double *h0,
-                    int64_t batch, int64_t L, int64_t D, int64_t N, int disc, int is_f64,
-                    const int64_t *chan, int64_t n_chan,
-                    double *y_out, double *state_out)
+int oracle_scan_fwd_ex(const void *x, const void *delta, const void *A_log,
+                       const void *B, const void *C, const double *h0,
+                       const double *delta_bias, int delta_softplus, const double *dskip, const void *z,
+                       int64_t batch, int64_t L, int64_t D, int64_t N, int disc, int is_f64,
+                       const int64_t *chan, int64_t n_chan,
+                       double *y_out, double *state_out)
 {
     if (batch < 0 || L < 0 || D < 0 || N < 1 || N > ORACLE_MAX_N) return -1;
     if (disc != ORACLE_EULER && disc != ORACLE_ZOH) return -1;
@@ -100,7 +129,7 @@ int oracle_scan_fwd(const void *x, const void *delta, const void *A_log,
         }
         for (int64_t t = 0; t < L; ++t) {
             double xt = ld(x, (b * L + t) * D + d, is_f64);
-            double dt = ld(delta, (b * L + t) * D + d, is_f64);
+            double dt = oracle_delta(ld(delta, (b * L + t) * D + d, is_f64), delta_bias, d, delta_softplus);
             int64_t bc = (b * L + t) * N;
             double yt = 0.0;
             for (int64_t n = 0; n < N; ++n) {
@@ -108,11 +137,21 @@ int oracle_scan_fwd(const void *x, const void *delta, const void *A_log,
                 h[n] = abar * h[n] + oracle_bbar_x(dt, A[n], ld(B, bc + n, is_f64), xt, disc);
                 yt += ld(C, bc + n, is_f64) * h[n];
             }
-            y_out[k * L + t] = yt;
+            y_out[k * L + t] = oracle_output(yt, xt, dskip, d, z, (b * L + t) * D + d, is_f64);
         }
         for (int64_t n = 0; n < N; ++n) state_out[k * N + n] = h[n];
     }
     return bad ? -1 : 0;
+}
+
+int oracle_scan_fwd(const void *x, const void *delta, const void *A_log,
+                    const void *B, const void *C, const double *h0,
+                    int64_t batch, int64_t L, int64_t D, int64_t N, int disc, int is_f64,
+                    const int64_t *chan, int64_t n_chan,
+                    double *y_out, double *state_out)
+{
+    return oracle_scan_fwd_ex(x, delta, A_log, B, C, h0, 0, 0, 0, 0, batch, L, D, N, disc, is_f64, chan, n_chan,
+                              y_out, state_out);
 }
 
 /*
@@ -120,10 +159,11 @@ int oracle_scan_fwd(const void *x, const void *delta, const void *A_log,
  * carried state). state: [n_chan, N] doubles, updated in place; x_t, delta_t: [batch, D];
  * B_t, C_t: [batch, N]; y_t: [n_chan].
  */
-int oracle_scan_step(double *state, const void *x_t, const void *delta_t, const void *A_log,
-                     const void *B_t, const void *C_t,
-                     int64_t batch, int64_t D, int64_t N, int disc, int is_f64,
-                     const int64_t *chan, int64_t n_chan, double *y_t)
+int oracle_scan_step_ex(double *state, const void *x_t, const void *delta_t, const void *A_log,
+                        const void *B_t, const void *C_t,
+                        const double *delta_bias, int delta_softplus, const double *dskip, const void *z_t,
+                        int64_t batch, int64_t D, int64_t N, int disc, int is_f64,
+                        const int64_t *chan, int64_t n_chan, double *y_t)
 {
     if (batch < 0 || D < 0 || N < 1 || N > ORACLE_MAX_N) return -1;
     if (disc != ORACLE_EULER && disc != ORACLE_ZOH) return -1;
@@ -135,7 +175,7 @@ int oracle_scan_step(double *state, const void *x_t, const void *delta_t, const 
         if (flat < 0 || flat >= batch * D) { bad = 1; continue; }
         int64_t b = flat / D, d = flat % D;
         double xt = ld(x_t, b * D + d, is_f64);
-        double dt = ld(delta_t, b * D + d, is_f64);
+        double dt = oracle_delta(ld(delta_t, b * D + d, is_f64), delta_bias, d, delta_softplus);
         double yt = 0.0;
         for (int64_t n = 0; n < N; ++n) {
             double A = -exp(ld(A_log, d * N + n, is_f64));
@@ -144,7 +184,16 @@ int oracle_scan_step(double *state, const void *x_t, const void *delta_t, const 
             state[k * N + n] = hn;
             yt += ld(C_t, b * N + n, is_f64) * hn;
         }
-        y_t[k] = yt;
+        y_t[k] = oracle_output(yt, xt, dskip, d, z_t, b * D + d, is_f64);
     }
     return bad ? -1 : 0;
+}
+
+int oracle_scan_step(double *state, const void *x_t, const void *delta_t, const void *A_log,
+                     const void *B_t, const void *C_t,
+                     int64_t batch, int64_t D, int64_t N, int disc, int is_f64,
+                     const int64_t *chan, int64_t n_chan, double *y_t)
+{
+    return oracle_scan_step_ex(state, x_t, delta_t, A_log, B_t, C_t, 0, 0, 0, 0, batch, D, N, disc, is_f64, chan,
+                               n_chan, y_t);
 }

@@ -344,9 +344,58 @@ def pin_split_and_step(orc):
             _close(ss[i], st[b, d], 0.0, "channel subset state")
 
 
+# --- layer pieces around the scan ------------------------------------------------------------------------
+
+def pin_softplus_inside_scan(orc):
+    """The chapter's 16-digit trace with Delta_t = softplus(x_t - 5) formed by the scan itself from the raw
+    projection x_t and the bias -5 ("Understanding Mamba" Eq. (6): softplus(b_Delta + w_Delta x_t)), for the
+    prefill and for four decode steps in a row."""
+    g = load("euler_scalar_trace.txt")
+    xs = np.asarray(g["x"], np.float64)
+    L = len(xs)
+    y, _ = orc.scan_fwd(_chan1(xs), _chan1(xs), np.zeros((1, 1)), _bc([[1.0]] * L), _bc([[1.0]] * L),
+                        disc="euler", f64=True, delta_bias=np.asarray(g["bias"], np.float64), delta_softplus=True)
+    _rel(y[0, :, 0], g["h"], 2e-15, "trace with in-scan softplus")
+    st = np.zeros((1, 1, 1))
+    hs = []
+    for t in range(L):
+        st, yt = orc.scan_step(st, xs[t].reshape(1, 1), xs[t].reshape(1, 1), np.zeros((1, 1)), np.ones((1, 1)),
+                               np.ones((1, 1)), disc="euler", f64=True, delta_bias=np.asarray(g["bias"], np.float64),
+                               delta_softplus=True)
+        hs.append(yt[0, 0])
+    _rel(hs, g["h"], 2e-15, "trace with in-step softplus")
+
+
+def pin_feedthrough_and_gate(orc):
+    """Closed forms of y_out = (C h + D x) * SiLU(z), SiLU(v) = v sigma(v) ("Understanding Mamba" Eq. (1)/(3),
+    s2.1: D is a direct pipe from x to the output, added after everything else; Eq. (9), s8.1: the gate)."""
+    rng = np.random.default_rng(3)
+    L = 5
+    x = rng.standard_normal(L)
+    z = rng.standard_normal(L)
+    ones, zeros = _bc([[1.0]] * L), _bc([[0.0]] * L)
+    dt = _chan1(np.full(L, 0.3))
+    # C = 0: the bucket never reaches the output, only the pipe does
+    y, _ = orc.scan_fwd(_chan1(x), dt, np.zeros((1, 1)), ones, zeros, disc="zoh", f64=True, D_skip=np.array([0.5]))
+    _close(y[0, :, 0], 0.5 * x, 1e-15, "feedthrough alone")
+    y, _ = orc.scan_fwd(_chan1(x), dt, np.zeros((1, 1)), ones, zeros, disc="zoh", f64=True, D_skip=np.array([0.5]),
+                        z=_chan1(z))
+    _close(y[0, :, 0], 0.5 * x * z / (1.0 + np.exp(-z)), 1e-15, "gated feedthrough")
+    # one step from rest: x = 1, raw delta 0 -> Delta = softplus(0) = ln 2, A = -1, B = C = 1, Euler: h = ln 2
+    y, _ = orc.scan_fwd(_chan1([1.0]), _chan1([0.0]), np.zeros((1, 1)), _bc([[1.0]]), _bc([[1.0]]), disc="euler",
+                        f64=True, delta_softplus=True, D_skip=np.array([0.5]), z=_chan1([1.0]))
+    _close(y[0, 0, 0], (0.5 + math.log(2.0)) / (1.0 + math.exp(-1.0)), 1e-15, "one gated step")
+    # SiLU(0) = 0 closes the gate; a large positive z passes y through, a large negative one blocks it
+    base, _ = orc.scan_fwd(_chan1(x), dt, np.zeros((1, 1)), ones, ones, disc="zoh", f64=True)
+    for zv, want in ((0.0, 0.0), (60.0, 60.0), (-60.0, 0.0)):
+        y, _ = orc.scan_fwd(_chan1(x), dt, np.zeros((1, 1)), ones, ones, disc="zoh", f64=True,
+                            z=_chan1(np.full(L, zv)))
+        _close(y[0, :, 0], base[0, :, 0] * want, 1e-12 * max(1.0, abs(want)), f"gate at z = {zv}")
+
+
 ALL_PINS = [
     pin_leaky_bucket_closed_form, pin_ema_identity, pin_euler_scalar_trace, pin_active_recall_traces,
     pin_lti_zoh_example, pin_convolution_view, pin_selective_zoh_example, pin_combine_tree,
     pin_small_delta_limit, pin_unit_input_two_step, pin_delta_limits, pin_brute_force_1ss,
-    pin_split_and_step,
+    pin_split_and_step, pin_softplus_inside_scan, pin_feedthrough_and_gate,
 ]

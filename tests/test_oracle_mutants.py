@@ -37,6 +37,11 @@ MUTANTS = {
     "step_reads_old_state": (
         "            state[k * N + n] = hn;\n            yt += ld(C_t, b * N + n, is_f64) * hn;",
         "            yt += ld(C_t, b * N + n, is_f64) * state[k * N + n];\n            state[k * N + n] = hn;"),
+    "softplus_dropped": ("    if (!softplus) return v;\n", "    return v;\n"),
+    "delta_bias_ignored": ("double v = raw + (bias ? bias[d] : 0.0);", "double v = raw;"),
+    "skip_dropped": ("double out = yssm + (dskip ? dskip[d] * x : 0.0);", "double out = yssm;"),
+    "gate_sigmoid_not_silu": ("out *= zv / (1.0 + exp(-zv));", "out *= 1.0 / (1.0 + exp(-zv));"),
+    "gate_sign_flipped": ("out *= zv / (1.0 + exp(-zv));", "out *= zv / (1.0 + exp(zv));"),
     "channel_index_swapped": ("int64_t b = flat / D, d = flat % D;\n        double h[",
                               "int64_t d = flat / D, b = flat % D;\n        double h["),
 }
