@@ -219,36 +219,60 @@ def _dev_tensor(torch, a, bf16):
     return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
 
 
-def measure_prefill(name, reps, flush, peak):
-    """Prefill of another workload, timed like the main one (L2 flushed before each launch, CUDA events)."""
+def measure_prefill(name, reps, flush, peak, fused=False):
+    """Prefill of another workload, timed like the main one (L2 flushed before each launch, CUDA events).
+    fused: the layer pieces around the scan as well -- delta = softplus(delta_raw + bias), y = (C h + D x) *
+    SiLU(z) -- with raw delta ~ N(mu, sigma) (the workload's law before its softplus), bias ~ U(-0.5, 0.5),
+    D ~ N(0, 1), z ~ N(0, 1); the gate input z adds one [batch, L, D] read."""
+    import ctypes
     import torch
     import selective_state_space_124_b300 as lib
+    from selective_state_space_124_b300 import _ffi
     cfg = dict(ssm_inputs.WORKLOADS[name])
     inp = ssm_inputs.workload_inputs(name)
     bf16 = cfg["dtype"] == "bf16"
-    d = {k: _dev_tensor(torch, inp[k], bf16) for k in ("x", "delta", "B", "C")}
-    A = torch.from_numpy(inp["A_log"].copy()).cuda()
     b, L, D, N = cfg["batch"], cfg["L"], cfg["D"], cfg["N"]
+    if fused:
+        rng = np.random.default_rng(99)
+        inp["delta"] = rng.normal(cfg["mu"], cfg["sigma"], (b, L, D)).astype(np.float32)
+        inp["z"] = rng.standard_normal((b, L, D)).astype(np.float32)
+    d = {k: _dev_tensor(torch, inp[k], bf16) for k in ("x", "delta", "B", "C") + (("z",) if fused else ())}
+    A = torch.from_numpy(inp["A_log"].copy()).cuda()
     y = torch.empty((b, L, D), dtype=torch.bfloat16 if bf16 else torch.float32, device="cuda")
     fs = torch.empty((b, D, N), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
-    args = (d["x"].data_ptr(), d["delta"].data_ptr(), A.data_ptr(), d["B"].data_ptr(), d["C"].data_ptr(), 0,
-            y.data_ptr(), fs.data_ptr(), b, L, D, N, cfg["dtype"], cfg["disc"], stream.cuda_stream)
+    if fused:
+        bias = torch.from_numpy(np.random.default_rng(98).uniform(-0.5, 0.5, D).astype(np.float32)).cuda()
+        dsk = torch.from_numpy(np.random.default_rng(97).standard_normal(D).astype(np.float32)).cuda()
+        v = ctypes.c_void_p
+        fn = _ffi.load().ssm_scan_fwd_ex
+        cargs = (v(d["x"].data_ptr()), v(d["delta"].data_ptr()), v(A.data_ptr()), v(d["B"].data_ptr()),
+                 v(d["C"].data_ptr()), None, v(bias.data_ptr()), 1, v(dsk.data_ptr()), v(d["z"].data_ptr()),
+                 v(y.data_ptr()), v(fs.data_ptr()), b, L, D, N, _ffi.DTYPE[cfg["dtype"]], _ffi.DISC[cfg["disc"]],
+                 v(stream.cuda_stream))
+        launch = lambda: _ffi.check("ssm_scan_fwd_ex", fn(*cargs))
+    else:
+        args = (d["x"].data_ptr(), d["delta"].data_ptr(), A.data_ptr(), d["B"].data_ptr(), d["C"].data_ptr(), 0,
+                y.data_ptr(), fs.data_ptr(), b, L, D, N, cfg["dtype"], cfg["disc"], stream.cuda_stream)
+        launch = lambda: lib.ssm_scan_fwd_ptr(*args)
     ms = []
     for i in range(3 + reps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        lib.ssm_scan_fwd_ptr(*args)
+        launch()
         e1.record(stream)
         torch.cuda.synchronize()
         if i >= 3:
             ms.append(e0.elapsed_time(e1))
     lib.check_device()
     med = statistics.median(ms) / 1e3
-    gbs = fwd_bytes(cfg) / med / 1e9
-    return {"workload": describe(name, cfg).split(";")[0], "launch_ms_median": med * 1e3,
-            "elems_per_s": b * L * D / med, "gbs": gbs, "hbm_frac": gbs / peak, "reps": reps}
+    es = 2 if bf16 else 4
+    nbytes = fwd_bytes(cfg) + ((b * L * D * es + 2 * D * 4) if fused else 0)  # + z, bias, D
+    gbs = nbytes / med / 1e9
+    what = describe(name, cfg).split(";")[0] + ("; fused softplus(delta + bias), + D x, * SiLU(z)" if fused else "")
+    return {"workload": what, "launch_ms_median": med * 1e3, "elems_per_s": b * L * D / med, "gbs": gbs,
+            "hbm_frac": gbs / peak, "bytes_per_launch": nbytes, "reps": reps}
 
 
 def measure_decode(steps, flush, peak):
@@ -543,6 +567,7 @@ def main(argv=None):
         for name in ("long", "mamba1p4b"):
             if name != args.workload:
                 extra[name] = measure_prefill(name, 10, flush, peak)
+        extra[args.workload + "_fused"] = measure_prefill(args.workload, 10, flush, peak, fused=True)
         extra["decode"] = measure_decode(1000, flush, peak)
         line["workloads"] = extra
     if not args.no_cpu_baseline:

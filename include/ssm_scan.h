@@ -83,6 +83,37 @@ ssm_status ssm_scan_step(float *state, const void *x_t, const void *delta_t, con
                          int64_t batch, int64_t D, int64_t N,
                          ssm_dtype dtype, ssm_disc disc, void *stream);
 
+/*
+ * Prefill scan with the layer pieces the pages define around it fused in ("Understanding Mamba" s5.1
+ * Eq. (6), s2.1 with Eq. (1)/(3), s8.1 Eq. (9)); every piece is optional:
+ *   delta_bias     [D]            fp32   b_Delta added to delta, or NULL (0)
+ *   delta_softplus                       nonzero: the scan uses softplus(delta + delta_bias[d]), where
+ *                                        softplus(v) = ln(1 + e^v); zero: delta + delta_bias[d] as given
+ *   D_skip         [D]            fp32   feedthrough D, or NULL (0)
+ *   z              [batch, L, D]  dtype  gate input, or NULL (no gate)
+ * and y[b,t,d] = (sum_n C[b,t,n] h[n] + D_skip[d] x[b,t,d]) * SiLU(z[b,t,d]), SiLU(v) = v / (1 + e^-v).
+ * The other arguments, the final state (which the gate and feedthrough do not touch) and the error
+ * behaviour are those of ssm_scan_fwd; z may not overlap an output. ssm_scan_fwd is this call with every
+ * piece off.
+ */
+ssm_status ssm_scan_fwd_ex(const void *x, const void *delta, const float *A_log,
+                           const void *B, const void *C, const float *h0,
+                           const float *delta_bias, int delta_softplus, const float *D_skip, const void *z,
+                           void *y, float *final_state,
+                           int64_t batch, int64_t L, int64_t D, int64_t N,
+                           ssm_dtype dtype, ssm_disc disc, void *stream);
+
+/*
+ * One decode step with the same optional pieces (z_t [batch, D] in `dtype`): the step of ssm_scan_step on
+ * delta = softplus(delta_t + delta_bias[d]) (or delta_t + delta_bias[d]), output
+ * y_t = (C_t . h + D_skip[d] x_t) * SiLU(z_t).
+ */
+ssm_status ssm_scan_step_ex(float *state, const void *x_t, const void *delta_t, const float *A_log,
+                            const void *B_t, const void *C_t,
+                            const float *delta_bias, int delta_softplus, const float *D_skip, const void *z_t,
+                            void *y_t, int64_t batch, int64_t D, int64_t N,
+                            ssm_dtype dtype, ssm_disc disc, void *stream);
+
 /* Synchronise `stream` and report any error raised while this library's kernels ran on it. */
 ssm_status ssm_check_device(void *stream);
 

@@ -3,6 +3,10 @@
     y, final_state = ssm_scan_fwd(x, delta, A_log, B, C, disc="euler" | "zoh", h0=None)
     y_t = ssm_scan_step(state, x_t, delta_t, A_log, B_t, C_t, disc=...)   # state updated in place
 
+Both take the layer pieces the library can fuse around the scan, each optional: ``delta_bias`` [D] and
+``delta_softplus`` (the scan uses softplus(delta + bias)), ``D_skip`` [D] (adds D x to y) and ``z`` (gates
+y by SiLU(z); [batch, L, D] for the prefill, ``z_t`` [batch, D] for a step).
+
 Arguments are torch tensors: x, delta [batch, L, D] and B, C [batch, L, N] in float32 or bfloat16
 (all four the same), A_log [D, N] float32, states float32. CUDA tensors run on the caller's current
 stream. CPU tensors are copied to the current CUDA device (asynchronously when pinned), processed, and
@@ -71,14 +75,27 @@ def _to_device(ts, device):
     return [None if t is None else t.to(device, non_blocking=True) for t in ts]
 
 
+def _check_extras(name, D, x, delta_bias, D_skip, z, z_shape):
+    torch = _torch()
+    for nm, t in (("delta_bias", delta_bias), ("D_skip", D_skip)):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (D,) or not t.is_contiguous()
+                              or t.device != x.device):
+            raise ValueError(f"{name}: {nm} must be a contiguous float32 [{D}] tensor on the inputs' device")
+    if z is not None and (z.dtype != x.dtype or tuple(z.shape) != z_shape or not z.is_contiguous()
+                          or z.device != x.device):
+        raise ValueError(f"{name}: z must be contiguous, {x.dtype}, shape {z_shape}, on the inputs' device")
+
+
 def ssm_scan_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, y=None, final_state=None,
-                 want_final_state: bool = True, stream=None):
+                 want_final_state: bool = True, stream=None, delta_bias=None, delta_softplus: bool = False,
+                 D_skip=None, z=None):
     """Prefill selective scan. Returns (y, final_state) (final_state None if not wanted)."""
     torch = _torch()
     if x.device.type == "cpu":
         dev = torch.device("cuda", torch.cuda.current_device())
-        xd, dd, ad, bd, cd, hd = _to_device([x, delta, A_log, B, C, h0], dev)
-        yd, fd = ssm_scan_fwd(xd, dd, ad, bd, cd, disc, hd, want_final_state=want_final_state, stream=stream)
+        xd, dd, ad, bd, cd, hd, bb, ds, zd = _to_device([x, delta, A_log, B, C, h0, delta_bias, D_skip, z], dev)
+        yd, fd = ssm_scan_fwd(xd, dd, ad, bd, cd, disc, hd, want_final_state=want_final_state, stream=stream,
+                              delta_bias=bb, delta_softplus=delta_softplus, D_skip=ds, z=zd)
         torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
         return yd.cpu(), None if fd is None else fd.cpu()
     batch, L, D = x.shape
@@ -95,19 +112,22 @@ def ssm_scan_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, y=None,
     ts = [x, delta, A_log, B, C] + ([h0] if h0 is not None else [])
     if any(not t.is_contiguous() for t in ts) or any(t.device != x.device for t in ts):
         raise ValueError("inputs must be contiguous and on one device")
+    _check_extras("ssm_scan_fwd", D, x, delta_bias, D_skip, z, (batch, L, D))
     if y is None:
         y = torch.empty((batch, L, D), dtype=x.dtype, device=x.device)
     if final_state is None and want_final_state:
         final_state = torch.empty((batch, D, N), dtype=torch.float32, device=x.device)
     s = stream if stream is not None else torch.cuda.current_stream(x.device)
-    st = _ffi.load().ssm_scan_fwd(_ptr(x), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(h0), _ptr(y),
-                                  _ptr(final_state), batch, L, D, N, code, _ffi.DISC[disc],
-                                  ctypes_void(s.cuda_stream))
+    st = _ffi.load().ssm_scan_fwd_ex(_ptr(x), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(h0),
+                                     _ptr(delta_bias), int(bool(delta_softplus)), _ptr(D_skip), _ptr(z), _ptr(y),
+                                     _ptr(final_state), batch, L, D, N, code, _ffi.DISC[disc],
+                                     ctypes_void(s.cuda_stream))
     _ffi.check("ssm_scan_fwd", st)
     return y, final_state
 
 
-def ssm_scan_step(state, x_t, delta_t, A_log, B_t, C_t, disc: str = "euler", *, y_t=None, stream=None):
+def ssm_scan_step(state, x_t, delta_t, A_log, B_t, C_t, disc: str = "euler", *, y_t=None, stream=None,
+                  delta_bias=None, delta_softplus: bool = False, D_skip=None, z_t=None):
     """One decode step: updates ``state`` [batch, D, N] in place and returns y_t [batch, D]."""
     torch = _torch()
     batch, D, N = state.shape
@@ -123,11 +143,13 @@ def ssm_scan_step(state, x_t, delta_t, A_log, B_t, C_t, disc: str = "euler", *, 
     ts = [state, x_t, delta_t, A_log, B_t, C_t]
     if any(not t.is_contiguous() for t in ts) or any(t.device != state.device for t in ts):
         raise ValueError("inputs must be contiguous and on one device")
+    _check_extras("ssm_scan_step", D, x_t, delta_bias, D_skip, z_t, (batch, D))
     if y_t is None:
         y_t = torch.empty((batch, D), dtype=x_t.dtype, device=state.device)
     s = stream if stream is not None else torch.cuda.current_stream(state.device)
-    st = _ffi.load().ssm_scan_step(_ptr(state), _ptr(x_t), _ptr(delta_t), _ptr(A_log), _ptr(B_t), _ptr(C_t),
-                                   _ptr(y_t), batch, D, N, code, _ffi.DISC[disc], ctypes_void(s.cuda_stream))
+    st = _ffi.load().ssm_scan_step_ex(_ptr(state), _ptr(x_t), _ptr(delta_t), _ptr(A_log), _ptr(B_t), _ptr(C_t),
+                                      _ptr(delta_bias), int(bool(delta_softplus)), _ptr(D_skip), _ptr(z_t),
+                                      _ptr(y_t), batch, D, N, code, _ffi.DISC[disc], ctypes_void(s.cuda_stream))
     _ffi.check("ssm_scan_step", st)
     return y_t
 

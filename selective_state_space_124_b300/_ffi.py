@@ -19,6 +19,10 @@ _vp, _i64, _i32, _fp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_v
 SIGNATURES = {
     "ssm_scan_fwd": (_i32, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i64, _i64, _i64, _i64, _i32, _i32, _vp]),
     "ssm_scan_step": (_i32, [_fp, _vp, _vp, _fp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
+    "ssm_scan_fwd_ex": (_i32, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _i32, _fp, _vp, _vp, _fp, _i64, _i64, _i64, _i64,
+                               _i32, _i32, _vp]),
+    "ssm_scan_step_ex": (_i32, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _i32, _fp, _vp, _vp, _i64, _i64, _i64, _i32, _i32,
+                                _vp]),
     "ssm_check_device": (_i32, [_vp]),
     "ssm_status_string": (ctypes.c_char_p, [_i32]),
     "ssm_last_error": (ctypes.c_char_p, []),

@@ -65,6 +65,14 @@ extern "C" {
 ssm_status ssm_scan_fwd(const void* x, const void* delta, const float* A_log, const void* B, const void* C,
                         const float* h0, void* y, float* final_state, int64_t batch, int64_t L, int64_t D,
                         int64_t N, ssm_dtype dtype, ssm_disc disc, void* stream) {
+  return ssm_scan_fwd_ex(x, delta, A_log, B, C, h0, nullptr, 0, nullptr, nullptr, y, final_state, batch, L, D, N,
+                         dtype, disc, stream);
+}
+
+ssm_status ssm_scan_fwd_ex(const void* x, const void* delta, const float* A_log, const void* B, const void* C,
+                           const float* h0, const float* delta_bias, int delta_softplus, const float* D_skip,
+                           const void* z, void* y, float* final_state, int64_t batch, int64_t L, int64_t D,
+                           int64_t N, ssm_dtype dtype, ssm_disc disc, void* stream) {
   g_last_error[0] = '\0';
   if (!valid_enums(dtype, disc)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: bad dtype or disc");
   if (batch < 0 || L < 0 || D < 0 || N < 1)
@@ -80,14 +88,20 @@ ssm_status ssm_scan_fwd(const void* x, const void* delta, const float* A_log, co
   if (bld > 0 && !A_log) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: null A_log");
   const Range ry = range_of(y, bld, es);
   const Range rf = range_of(final_state, final_state ? bdn : 0, 4);
-  const Range ins[] = {range_of(x, bld, es), range_of(delta, bld, es), range_of(A_log, D * N, 4),
-                       range_of(B, bln, es), range_of(C, bln, es), range_of(h0, h0 ? bdn : 0, 4)};
+  const Range ins[] = {range_of(x, bld, es),        range_of(delta, bld, es),  range_of(A_log, D * N, 4),
+                       range_of(B, bln, es),        range_of(C, bln, es),      range_of(h0, h0 ? bdn : 0, 4),
+                       range_of(delta_bias, delta_bias ? D : 0, 4), range_of(D_skip, D_skip ? D : 0, 4),
+                       range_of(z, z ? bld : 0, es)};
   for (const Range& r : ins)
     if (overlap(ry, r) || overlap(rf, r)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: outputs overlap inputs");
   if (overlap(ry, rf)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd: y overlaps final_state");
 
   FwdArgs a{x, delta, A_log, B, C, h0, y, final_state, batch, L, D, N, static_cast<int>(dtype),
             static_cast<int>(disc), static_cast<cudaStream_t>(stream)};
+  a.delta_bias = delta_bias;
+  a.softplus = delta_softplus != 0;
+  a.D_skip = D_skip;
+  a.z = z;
   if (batch == 0 || D == 0) return SSM_OK;
   cudaError_t e = (L == 0) ? launch_init_state(a) : (tma_path_ok(a) ? launch_fwd_tma(a) : launch_fwd_simple(a));
   if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd launch");
@@ -97,6 +111,14 @@ ssm_status ssm_scan_fwd(const void* x, const void* delta, const float* A_log, co
 ssm_status ssm_scan_step(float* state, const void* x_t, const void* delta_t, const float* A_log,
                          const void* B_t, const void* C_t, void* y_t, int64_t batch, int64_t D, int64_t N,
                          ssm_dtype dtype, ssm_disc disc, void* stream) {
+  return ssm_scan_step_ex(state, x_t, delta_t, A_log, B_t, C_t, nullptr, 0, nullptr, nullptr, y_t, batch, D, N, dtype,
+                          disc, stream);
+}
+
+ssm_status ssm_scan_step_ex(float* state, const void* x_t, const void* delta_t, const float* A_log,
+                            const void* B_t, const void* C_t, const float* delta_bias, int delta_softplus,
+                            const float* D_skip, const void* z_t, void* y_t, int64_t batch, int64_t D, int64_t N,
+                            ssm_dtype dtype, ssm_disc disc, void* stream) {
   g_last_error[0] = '\0';
   if (!valid_enums(dtype, disc)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_step: bad dtype or disc");
   if (batch < 0 || D < 0 || N < 1)
@@ -111,12 +133,17 @@ ssm_status ssm_scan_step(float* state, const void* x_t, const void* delta_t, con
   const int64_t es = dtype == SSM_DTYPE_BF16 ? 2 : 4;
   const Range rs = range_of(state, bdn, 4), ry = range_of(y_t, bd, es);
   const Range ins[] = {range_of(x_t, bd, es), range_of(delta_t, bd, es), range_of(A_log, D * N, 4),
-                       range_of(B_t, bn, es), range_of(C_t, bn, es)};
+                       range_of(B_t, bn, es), range_of(C_t, bn, es), range_of(delta_bias, delta_bias ? D : 0, 4),
+                       range_of(D_skip, D_skip ? D : 0, 4), range_of(z_t, z_t ? bd : 0, es)};
   for (const Range& r : ins)
     if (overlap(rs, r) || overlap(ry, r)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_step: outputs overlap inputs");
   if (overlap(rs, ry)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_step: y_t overlaps state");
   StepArgs a{state, x_t, delta_t, A_log, B_t, C_t, y_t, batch, D, N, static_cast<int>(dtype),
              static_cast<int>(disc), static_cast<cudaStream_t>(stream)};
+  a.delta_bias = delta_bias;
+  a.softplus = delta_softplus != 0;
+  a.D_skip = D_skip;
+  a.z = z_t;
   cudaError_t e = launch_step(a);
   if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_step launch");
   return SSM_OK;

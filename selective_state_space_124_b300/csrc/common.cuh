@@ -31,6 +31,35 @@ __device__ __forceinline__ float exp2m1(float w, float a) {
   return fabsf(w) < 0.04508422002825452f ? q : a - 1.0f;
 }
 
+// Reciprocal with the SFU approximation (relative error about one ulp; rcp(inf) = 0).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// log(1 + u) for u in [0, 1] from the identity log(1 + u) = 2 artanh(s), s = u / (2 + u) <= 1/3, and the
+// artanh series s + s^3/3 + ... + s^13/13 (the next term is below 5e-9 relative).
+__device__ __forceinline__ float log1p_unit(float u) {
+  const float s = u * rcp_approx(2.0f + u);
+  const float t = s * s;
+  float q = fmaf(t, 1.0f / 13.0f, 1.0f / 11.0f);
+  q = fmaf(t, q, 1.0f / 9.0f);
+  q = fmaf(t, q, 1.0f / 7.0f);
+  q = fmaf(t, q, 1.0f / 5.0f);
+  q = fmaf(t, q, 1.0f / 3.0f);
+  q = fmaf(t, q, 1.0f);
+  return 2.0f * s * q;
+}
+
+// softplus(v) = ln(1 + e^v) = max(v, 0) + log(1 + e^{-|v|}), with no overflow for large v.
+__device__ __forceinline__ float softplus_f(float v) {
+  return fmaxf(v, 0.0f) + log1p_unit(ex2(-fabsf(v) * kLog2e));
+}
+
+// SiLU(v) = v * sigma(v) = v / (1 + e^{-v}).
+__device__ __forceinline__ float silu_f(float v) { return v * rcp_approx(1.0f + ex2(-v * kLog2e)); }
+
 template <typename T> struct Elem;
 template <> struct Elem<float> {
   __device__ __forceinline__ static float load(const void* p, int64_t i) {

@@ -18,6 +18,11 @@ struct FwdArgs {
   int dtype;  // 0 f32, 1 bf16
   int disc;   // 0 euler, 1 zoh
   cudaStream_t stream;
+  // optional layer pieces (all off: the plain scan)
+  const float* delta_bias = nullptr;  // [D]
+  int softplus = 0;                   // delta = softplus(delta + bias)
+  const float* D_skip = nullptr;      // [D]
+  const void* z = nullptr;            // [batch, L, D] (dtype): y = (y + D x) * SiLU(z)
 };
 
 struct StepArgs {
@@ -32,6 +37,10 @@ struct StepArgs {
   int dtype;
   int disc;
   cudaStream_t stream;
+  const float* delta_bias = nullptr;  // [D]
+  int softplus = 0;
+  const float* D_skip = nullptr;      // [D]
+  const void* z = nullptr;            // [batch, D] (dtype)
 };
 
 int sm_count();  // multiprocessors of the current device (cached per device)

@@ -37,7 +37,17 @@ struct SimpleParams {
   int64_t groups;   // ceil(D / 32)
   int64_t total;    // batch * groups * L
   int64_t nwarps;   // warps taking part
+  // optional layer pieces (see ssm_scan_fwd_ex); applied with warp-uniform branches
+  const float* delta_bias;  // [D] or null: delta + bias[d]
+  int softplus;             // delta = softplus(delta + bias[d])
+  const float* D_skip;      // [D] or null: y + D[d] x
+  const void* z;            // [batch, L, D] or null: y * SiLU(z)
 };
+
+__device__ __forceinline__ float delta_of(const SimpleParams& p, float raw, float bias) {
+  const float v = raw + bias;
+  return p.softplus ? softplus_f(v) : v;
+}
 
 template <int NP, bool ZOH>
 struct Chan {
@@ -76,6 +86,8 @@ __global__ void __launch_bounds__(kWarps * 32) scan_fwd_simple_kernel(SimplePara
     const int64_t b = row / p.groups;
     const int64_t d = (row % p.groups) * 32 + lane;
     const bool act = d < p.D;
+    const float dbias = (act && p.delta_bias) ? __ldg(p.delta_bias + d) : 0.0f;
+    const float dskip = (act && p.D_skip) ? __ldg(p.D_skip + d) : 0.0f;
 
     Chan<NP, ZOH> c;
 #pragma unroll
@@ -107,7 +119,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_fwd_simple_kernel(SimplePara
       while (true) {
         const int64_t xi = (b * p.L + j) * p.D + d;
         const float xv = act ? Elem<T>::load(p.x, xi) : 0.0f;
-        const float dt = act ? Elem<T>::load(p.delta, xi) : 0.0f;
+        const float dt = act ? delta_of(p, Elem<T>::load(p.delta, xi), dbias) : 0.0f;
         const int64_t bi = (b * p.L + j) * N;
 #pragma unroll
         for (int n = 0; n < NP; ++n) {
@@ -141,7 +153,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_fwd_simple_kernel(SimplePara
     for (int64_t t = t0; t < t1; ++t) {
       const int64_t xi = (b * p.L + t) * p.D + d;
       const float xv = act ? Elem<T>::load(p.x, xi) : 0.0f;
-      const float dt = act ? Elem<T>::load(p.delta, xi) : 0.0f;
+      const float dt = act ? delta_of(p, Elem<T>::load(p.delta, xi), dbias) : 0.0f;
       const int64_t bi = (b * p.L + t) * N;
       float yv = 0.0f;
 #pragma unroll
@@ -153,7 +165,11 @@ __global__ void __launch_bounds__(kWarps * 32) scan_fwd_simple_kernel(SimplePara
         h[n] = fmaf(e, h[n], h[n]) + bx;
         yv = fmaf(cn, h[n], yv);
       }
-      if (act) Elem<T>::store(p.y, xi, yv);
+      if (act) {
+        if (p.D_skip) yv = fmaf(dskip, xv, yv);
+        if (p.z) yv *= silu_f(Elem<T>::load(p.z, xi));
+        Elem<T>::store(p.y, xi, yv);
+      }
     }
     if (t1 == p.L && p.final_state && act) {
       float* fs = p.final_state + (b * p.D + d) * N;
@@ -189,6 +205,7 @@ cudaError_t launch_fwd_simple(const FwdArgs& a) {
   SimpleParams sp;
   sp.x = a.x; sp.delta = a.delta; sp.A_log = a.A_log; sp.B = a.B; sp.C = a.C; sp.h0 = a.h0;
   sp.y = a.y; sp.final_state = a.final_state;
+  sp.delta_bias = a.delta_bias; sp.softplus = a.softplus; sp.D_skip = a.D_skip; sp.z = a.z;
   sp.batch = a.batch; sp.L = a.L; sp.D = a.D; sp.N = a.N;
   sp.groups = (a.D + 31) / 32;
   const int64_t rows = a.batch * sp.groups;

@@ -81,6 +81,11 @@ struct TmaParams {
   int64_t G;        // channel groups (of 32 * CPL channels) per batch element
   int64_t total;    // batch * G * L
   int64_t nwarps;   // warps taking part
+  // fused layer pieces (see ssm_scan_fwd_ex). Kept after the fields above: placed before them, the long
+  // fp32 ZOH scan measured 4% slower with the same registers and instruction mix.
+  const float* delta_bias;  // [D] or null
+  const float* D_skip;      // [D] or null
+  const void* z;            // [batch, L, D] or null
 };
 
 // ---- PTX wrappers -----------------------------------------------------------------------------------
@@ -228,13 +233,30 @@ __device__ __forceinline__ void gen_pair(const ChanGen& g, int k, float dv, floa
   }
 }
 
+// ---- fused layer pieces --------------------------------------------------------------------------------
+// DX: how the scan reads delta. 0: as given; 2: softplus(delta + bias[d]) ("Understanding Mamba" Eq. (6)).
+// EPI: 0: y as read out; 1: y + D[d] x (Eq. (1)/(3) feedthrough); 2: (y + D[d] x) * SiLU(z) (Eq. (9) gate).
+template <int DX>
+__device__ __forceinline__ float delta_in(float raw, float bias) {
+  if (DX == 2) return softplus_f(raw + bias);
+  if (DX == 1) return raw + bias;
+  return raw;
+}
+template <int EPI>
+__device__ __forceinline__ float epilogue(float y, float x, float dskip, float z) {
+  if (EPI == 0) return y;
+  const float v = fmaf(dskip, x, y);
+  return EPI == 2 ? v * silu_f(z) : v;
+}
+
 // ---- backward warm-up over one staged tile (rows i = n-1 .. 0 of the tile, i.e. steps hi-1 .. lo) -------
 // Structured A, NP pairs active. W[c] is log2 of the decay of entry 0 of channel c over the steps after the
 // current one (running sum of delta * A_0 log2 e); P[c] holds the matching decay weights of the active pairs.
-template <int NP, bool ZOH, int CPL, typename T>
+template <int NP, bool ZOH, int CPL, int DX, typename T>
 __device__ __forceinline__ void warm_s4d_step(const T* xs, const T* ds, const T* Bs, int i, int lane,
-                                              const float (&A2_0)[CPL], const float (&invA0)[CPL], float (&W)[CPL],
-                                              float2 (&P)[CPL][8], float2 (&h)[CPL][8]) {
+                                              const float (&A2_0)[CPL], const float (&invA0)[CPL],
+                                              const float (&dbias)[CPL], float (&W)[CPL], float2 (&P)[CPL][8],
+                                              float2 (&h)[CPL][8]) {
   constexpr int CW = 32 * CPL;
   const T* Brow = Bs + i * 16;
   float2 bp[NP];
@@ -243,7 +265,7 @@ __device__ __forceinline__ void warm_s4d_step(const T* xs, const T* ds, const T*
 #pragma unroll
   for (int c = 0; c < CPL; ++c) {
     const float xv = tof<T>(xs[i * CW + c * 32 + lane]);
-    const float dv = tof<T>(ds[i * CW + c * 32 + lane]);
+    const float dv = delta_in<DX>(tof<T>(ds[i * CW + c * 32 + lane]), dbias[c]);
     const float w = dv * A2_0[c];
     if (ZOH) {
       // contribution P_n (Abar_n - 1) / A_n B_n x = (P_n e_n) B_n (x / A_0) / (n + 1); the 1/(n+1) is applied
@@ -264,24 +286,27 @@ __device__ __forceinline__ void warm_s4d_step(const T* xs, const T* ds, const T*
   }
 }
 
-template <int NP, bool ZOH, int CPL, int TS, typename T>
+template <int NP, bool ZOH, int CPL, int TS, int DX, typename T>
 __device__ __forceinline__ void warm_s4d(const T* xs, const T* ds, const T* Bs, int n, int lane,
-                                         const float (&A2_0)[CPL], const float (&invA0)[CPL], float (&W)[CPL],
-                                         float2 (&P)[CPL][8], float2 (&h)[CPL][8]) {
+                                         const float (&A2_0)[CPL], const float (&invA0)[CPL],
+                                         const float (&dbias)[CPL], float (&W)[CPL], float2 (&P)[CPL][8],
+                                         float2 (&h)[CPL][8]) {
   if (n == TS) {
 #pragma unroll
-    for (int i = TS - 1; i >= 0; --i) warm_s4d_step<NP, ZOH, CPL>(xs, ds, Bs, i, lane, A2_0, invA0, W, P, h);
+    for (int i = TS - 1; i >= 0; --i)
+      warm_s4d_step<NP, ZOH, CPL, DX>(xs, ds, Bs, i, lane, A2_0, invA0, dbias, W, P, h);
   } else {
 #pragma unroll 1
-    for (int i = n - 1; i >= 0; --i) warm_s4d_step<NP, ZOH, CPL>(xs, ds, Bs, i, lane, A2_0, invA0, W, P, h);
+    for (int i = n - 1; i >= 0; --i)
+      warm_s4d_step<NP, ZOH, CPL, DX>(xs, ds, Bs, i, lane, A2_0, invA0, dbias, W, P, h);
   }
 }
 
 // Generic A, all pairs. S[c] is the running sum of delta over the steps after the current one.
-template <bool ZOH, int CPL, typename T>
+template <bool ZOH, int CPL, int DX, typename T>
 __device__ __forceinline__ void warm_gen(const T* xs, const T* ds, const T* Bs, int n, int lane,
-                                         const ChanGen (&g)[CPL], float (&S)[CPL], float2 (&P)[CPL][8],
-                                         float2 (&h)[CPL][8]) {
+                                         const ChanGen (&g)[CPL], const float (&dbias)[CPL], float (&S)[CPL],
+                                         float2 (&P)[CPL][8], float2 (&h)[CPL][8]) {
   constexpr int CW = 32 * CPL;
 #pragma unroll 1
   for (int i = n - 1; i >= 0; --i) {
@@ -289,7 +314,7 @@ __device__ __forceinline__ void warm_gen(const T* xs, const T* ds, const T* Bs, 
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
       const float xv = tof<T>(xs[i * CW + c * 32 + lane]);
-      const float dv = tof<T>(ds[i * CW + c * 32 + lane]);
+      const float dv = delta_in<DX>(tof<T>(ds[i * CW + c * 32 + lane]), dbias[c]);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         float2 e, bx;
@@ -311,6 +336,7 @@ __device__ __forceinline__ void warm_gen(const T* xs, const T* ds, const T* Bs, 
 template <bool ZOH, int CPL>
 __device__ __forceinline__ void fwd_prep(const float (&xv)[CPL], const float (&dv)[CPL], const float (&A2_0)[CPL],
                                          const float (&invA0)[CPL], float2 (&e)[CPL][8], float2 (&s)[CPL]) {
+  // dv is the delta the recurrence uses (already through delta_in)
 #pragma unroll
   for (int c = 0; c < CPL; ++c) {  // s: x / A_0 (ZOH) or delta * x (Euler)
     const float w = dv[c] * A2_0[c];
@@ -425,7 +451,8 @@ __device__ __forceinline__ int warm_prologue(WarpRing<T, CPL, TS, NSF, TSW, NSW>
 // One piece of a warp's range: row (batch b, channel group), steps [t0, t1). Warm-up (t0 > 0), forward with
 // y stores, final state (t1 == L). S4D selects the structured-A arithmetic at compile time, so the two
 // paths do not hold each other's per-channel constants in registers. Returns false if a wait ran out.
-template <bool S4D, typename T, bool ZOH, int CPL, int TS, int NSF, int TSW, int NSW, typename IssueFwd>
+template <bool S4D, typename T, bool ZOH, int CPL, int TS, int NSF, int TSW, int NSW, int DX, int EPI,
+          typename IssueFwd>
 __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r, const TmaParams& p,
                                           const CUtensorMap* mx, const CUtensorMap* md, const CUtensorMap* mB,
                                           int lane, int64_t row, int64_t t0, int64_t t1, WarpPipe& wp,
@@ -442,6 +469,13 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
   const bool full = (row % p.G) * CW + CW <= p.D;  // every channel of the warp exists
 
   // ---- per-channel constants ----
+  float dbias[CPL], dskip[CPL];  // fused pieces: delta bias, feedthrough D (0 where not given)
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const int64_t d = d0 + 32 * c;
+    dbias[c] = (DX != 0 && act[c] && p.delta_bias) ? __ldg(p.delta_bias + d) : 0.0f;
+    dskip[c] = (EPI != 0 && act[c] && p.D_skip) ? __ldg(p.D_skip + d) : 0.0f;
+  }
   float A2_0[CPL], invA0[CPL];  // structured: A_0 log2(e), 1 / A_0
   ChanGen g[S4D ? 1 : CPL];     // generic: every entry's rate
 #pragma unroll
@@ -524,12 +558,12 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
       const T* ds = r.wd[slot];
       const T* Bs = r.wB[slot];
       if constexpr (S4D) {
-        if (np == 8) warm_s4d<8, ZOH, CPL, TSW>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
-        else if (np == 4) warm_s4d<4, ZOH, CPL, TSW>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
-        else if (np == 2) warm_s4d<2, ZOH, CPL, TSW>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
-        else warm_s4d<1, ZOH, CPL, TSW>(xs, ds, Bs, n, lane, A2_0, invA0, W, P, h);
+        if (np == 8) warm_s4d<8, ZOH, CPL, TSW, DX>(xs, ds, Bs, n, lane, A2_0, invA0, dbias, W, P, h);
+        else if (np == 4) warm_s4d<4, ZOH, CPL, TSW, DX>(xs, ds, Bs, n, lane, A2_0, invA0, dbias, W, P, h);
+        else if (np == 2) warm_s4d<2, ZOH, CPL, TSW, DX>(xs, ds, Bs, n, lane, A2_0, invA0, dbias, W, P, h);
+        else warm_s4d<1, ZOH, CPL, TSW, DX>(xs, ds, Bs, n, lane, A2_0, invA0, dbias, W, P, h);
       } else {
-        warm_gen<ZOH, CPL>(xs, ds, Bs, n, lane, g, W, P, h);
+        warm_gen<ZOH, CPL, DX>(xs, ds, Bs, n, lane, g, dbias, W, P, h);
       }
       ++wp.wcon;
       // Pair k holds entries 2k, 2k+1 whose log2 decay is (2k+1) W, (2k+2) W (structured). A pair is
@@ -605,6 +639,7 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
     const float* Bs = kConv ? r.Bf : reinterpret_cast<const float*>(r.fB[slot]);
     const float* Cs = kConv ? r.Cf : reinterpret_cast<const float*>(r.fC[slot]);
     T* yp = static_cast<T*>(p.y) + (b * L + tb) * p.D + d0;  // channel c at yp + 32 c
+    const T* zp = EPI == 2 ? static_cast<const T*>(p.z) + (b * L + tb) * p.D + d0 : nullptr;  // gate input
     if constexpr (S4D) {
       auto one = [&](auto all_active, int i) {
         float xv[CPL], dv[CPL], yv[CPL];
@@ -613,9 +648,13 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
           xv[c] = tof<T>(xs[i * CW + c * 32 + lane]);
           dv[c] = tof<T>(ds[i * CW + c * 32 + lane]);
         }
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) dv[c] = delta_in<DX>(dv[c], dbias[c]);
         fwd_s4d<ZOH, CPL>(xv, dv, Bs + i * 16, Cs + i * 16, A2_0, invA0, h, yv);
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
+          const float zv = (EPI == 2 && act[c]) ? tof<T>(zp[static_cast<int64_t>(i) * p.D + 32 * c]) : 0.0f;
+          yv[c] = epilogue<EPI>(yv[c], xv[c], dskip[c], zv);
           if constexpr (decltype(all_active)::value) store_y(yp + 32 * c, yv[c]);
           else store_y(yp + 32 * c, yv[c], act[c]);
         }
@@ -627,12 +666,19 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
       constexpr bool kPipe = sizeof(T) == 4;
       if (kPipe && n == TS && full) {
         float2 e[CPL][8], s2[CPL];
+        float zt[EPI == 2 ? TS : 1][CPL];  // gate inputs of the stage, loaded up front
+        if constexpr (EPI == 2) {
+#pragma unroll
+          for (int i = 0; i < TS; ++i)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) zt[i][c] = tof<T>(zp[static_cast<int64_t>(i) * p.D + 32 * c]);
+        }
         auto prep = [&](int i, float2 (&ee)[CPL][8], float2 (&ss)[CPL]) {
           float xv[CPL], dv[CPL];
 #pragma unroll
           for (int c = 0; c < CPL; ++c) {
             xv[c] = tof<T>(xs[i * CW + c * 32 + lane]);
-            dv[c] = tof<T>(ds[i * CW + c * 32 + lane]);
+            dv[c] = delta_in<DX>(tof<T>(ds[i * CW + c * 32 + lane]), dbias[c]);
           }
           fwd_prep<ZOH, CPL>(xv, dv, A2_0, invA0, ee, ss);
         };
@@ -644,7 +690,11 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
           float yv[CPL];
           fwd_core<ZOH, CPL>(e, s2, Bs + i * 16, Cs + i * 16, h, yv);
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) store_y(yp + 32 * c, yv[c]);
+          for (int c = 0; c < CPL; ++c) {
+            if constexpr (EPI != 0)  // x of this step re-read from the stage for the feedthrough
+              yv[c] = epilogue<EPI>(yv[c], tof<T>(xs[i * CW + c * 32 + lane]), dskip[c], EPI == 2 ? zt[i][c] : 0.0f);
+            store_y(yp + 32 * c, yv[c]);
+          }
           yp += p.D;
           if (i + 1 < TS) {
 #pragma unroll
@@ -670,9 +720,11 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
       for (int i = 0; i < n; ++i) {
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-          const float yv = fwd_gen<ZOH>(tof<T>(xs[i * CW + c * 32 + lane]), tof<T>(ds[i * CW + c * 32 + lane]),
+          const float xv = tof<T>(xs[i * CW + c * 32 + lane]);
+          const float yv = fwd_gen<ZOH>(xv, delta_in<DX>(tof<T>(ds[i * CW + c * 32 + lane]), dbias[c]),
                                         Bs + i * 16, Cs + i * 16, g[S4D ? 0 : c], h[c]);
-          store_y(yp + 32 * c, yv, act[c]);
+          const float zv = (EPI == 2 && act[c]) ? tof<T>(zp[static_cast<int64_t>(i) * p.D + 32 * c]) : 0.0f;
+          store_y(yp + 32 * c, epilogue<EPI>(yv, xv, dskip[c], zv), act[c]);
         }
         yp += p.D;
       }
@@ -694,7 +746,7 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
   return true;
 }
 
-template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int TSW, int NSW>
+template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int TSW, int NSW, int DX, int EPI>
 __global__ void __launch_bounds__(NW * 32, 1)
 scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap md,
                     const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mC,
@@ -809,8 +861,8 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
       }
     }
     const bool alive = __all_sync(0xffffffffu, ok)
-                           ? run_piece<true, T, ZOH, CPL, TS, NSF, TSW, NSW>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0)
-                           : run_piece<false, T, ZOH, CPL, TS, NSF, TSW, NSW>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0);
+                           ? run_piece<true, T, ZOH, CPL, TS, NSF, TSW, NSW, DX, EPI>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0)
+                           : run_piece<false, T, ZOH, CPL, TS, NSF, TSW, NSW, DX, EPI>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0);
     if (!alive) break;
   }
 
@@ -858,7 +910,7 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint6
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int TSW, int NSW>
+template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int TSW, int NSW, int DX, int EPI>
 cudaError_t launch_cfg(const FwdArgs& a) {
   constexpr int CW = 32 * CPL;
   const bool bf16 = sizeof(T) == 2;
@@ -872,6 +924,9 @@ cudaError_t launch_cfg(const FwdArgs& a) {
   TmaParams p;
   p.A_log = a.A_log;
   p.h0 = a.h0;
+  p.delta_bias = a.delta_bias;
+  p.D_skip = a.D_skip;
+  p.z = a.z;
   p.y = a.y;
   p.final_state = a.final_state;
   p.L = a.L;
@@ -879,7 +934,7 @@ cudaError_t launch_cfg(const FwdArgs& a) {
   p.G = (a.D + CW - 1) / CW;
   p.total = a.batch * p.G * a.L;
   const size_t smem = sizeof(WarpRing<T, CPL, TS, NSF, TSW, NSW>) * NW + 128;
-  auto kern = scan_fwd_tma_kernel<T, ZOH, CPL, NW, TS, NSF, TSW, NSW>;
+  auto kern = scan_fwd_tma_kernel<T, ZOH, CPL, NW, TS, NSF, TSW, NSW, DX, EPI>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -919,15 +974,31 @@ struct ShapeAlt { static constexpr int CPL = 2, NW = 8, TS = 8, NSF = 3, TSW = 8
 #define SSM_SHAPE_BF16 ShapeBF16
 #endif
 
+template <typename T, bool ZOH, typename S, int DX, int EPI>
+cudaError_t launch_fused(const FwdArgs& a) {
+  return launch_cfg<T, ZOH, S::CPL, S::NW, S::TS, S::NSF, S::TSW, S::NSW, DX, EPI>(a);
+}
+
+// The plain scan, and softplus(delta + bias) with the feedthrough alone or with the gate (the layer's usual
+// combinations); other combinations go to the general kernel.
 template <typename T, bool ZOH, typename S>
 cudaError_t launch_shape(const FwdArgs& a) {
-  return launch_cfg<T, ZOH, S::CPL, S::NW, S::TS, S::NSF, S::TSW, S::NSW>(a);
+  const int dx = a.softplus ? 2 : 0;
+  const int epi = a.z ? 2 : (a.D_skip || a.softplus) ? 1 : 0;
+  if (dx == 0 && epi == 0) return launch_fused<T, ZOH, S, 0, 0>(a);
+  if (dx == 2 && epi == 1) return launch_fused<T, ZOH, S, 2, 1>(a);
+  if (dx == 2 && epi == 2) return launch_fused<T, ZOH, S, 2, 2>(a);
+  return cudaErrorNotSupported;  // tma_path_ok() keeps other combinations away
 }
 
 }  // namespace
 
 bool tma_path_ok(const FwdArgs& a) {
   if (a.N != 16) return false;
+  // fused combinations this kernel is built for: none, or softplus(delta + bias) with the feedthrough
+  // (D_skip or none) and optionally the gate
+  const bool plain = !a.softplus && !a.delta_bias && !a.D_skip && !a.z;
+  if (!plain && !a.softplus) return false;
   const int es = a.dtype == 1 ? 2 : 4;
   if ((a.D * es) % 16 != 0) return false;
   const void* ptrs[] = {a.x, a.delta, a.B, a.C};

@@ -22,7 +22,24 @@ struct StepParams {
   const void* C;
   void* y;
   int64_t batch, D, N;
+  // optional layer pieces (see ssm_scan_step_ex); warp-uniform branches on the pointers / flag
+  const float* delta_bias;  // [D] or null
+  int softplus;
+  const float* D_skip;      // [D] or null
+  const void* z;            // [batch, D] or null
 };
+
+__device__ __forceinline__ float step_delta(const StepParams& p, float raw, int64_t d) {
+  const float v = p.delta_bias ? raw + __ldg(p.delta_bias + d) : raw;
+  return p.softplus ? softplus_f(v) : v;
+}
+
+template <typename T>
+__device__ __forceinline__ float step_output(const StepParams& p, float y, float x, int64_t ch, int64_t d) {
+  if (p.D_skip) y = fmaf(__ldg(p.D_skip + d), x, y);
+  if (p.z) y *= silu_f(Elem<T>::load(p.z, ch));
+  return y;
+}
 
 // ---- N = 16: four lanes per channel ---------------------------------------------------------------------
 template <typename T> struct Vec4;
@@ -62,7 +79,7 @@ struct QuadIn {  // one lane's share of a channel: four state entries and their 
   float xv, dt;
 };
 
-template <typename T>
+template <bool FUSED, typename T>
 __device__ __forceinline__ void quad_load(const StepParams& p, int64_t ch, int q, QuadIn& v) {
   // batch * D < 2^31 is checked on the host: a 32-bit division is a short sequence, a 64-bit one is not
   const uint32_t b32 = static_cast<uint32_t>(ch) / static_cast<uint32_t>(p.D);
@@ -73,6 +90,7 @@ __device__ __forceinline__ void quad_load(const StepParams& p, int64_t ch, int q
   v.cc = Vec4<T>::load(p.C, b * 16 + 4 * q);
   v.xv = Elem<T>::load(p.x, ch);
   v.dt = Elem<T>::load(p.delta, ch);
+  if (FUSED) v.dt = step_delta(p, v.dt, d);
 }
 
 template <bool ZOH>
@@ -86,8 +104,9 @@ __device__ __forceinline__ float quad_step(QuadIn& v) {
 }
 
 // Persistent grid over the (channel, quad) items; each trip handles two items, both loaded before either is
-// computed, so that every lane keeps two state rows' worth of loads in flight.
-template <bool ZOH, typename T>
+// computed, so that every lane keeps two state rows' worth of loads in flight. FUSED = any of the optional
+// layer pieces is present; without them the kernel carries none of their loads or branches.
+template <bool ZOH, bool FUSED, typename T>
 __global__ void __launch_bounds__(256) scan_step_quad_kernel(StepParams p, int64_t quads) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t span = 2 * stride;
@@ -97,8 +116,8 @@ __global__ void __launch_bounds__(256) scan_step_quad_kernel(StepParams p, int64
     const bool live0 = i0 < quads, live1 = i1 < quads;
     const int q = static_cast<int>(i0 & 3);  // stride is a multiple of 4: both items use entries 4q .. 4q+3
     QuadIn v0, v1;
-    if (live0) quad_load<T>(p, i0 >> 2, q, v0);
-    if (live1) quad_load<T>(p, i1 >> 2, q, v1);
+    if (live0) quad_load<FUSED, T>(p, i0 >> 2, q, v0);
+    if (live1) quad_load<FUSED, T>(p, i1 >> 2, q, v1);
     float y0 = 0.0f, y1 = 0.0f;
     if (live0) {
       y0 = quad_step<ZOH>(v0);
@@ -112,6 +131,11 @@ __global__ void __launch_bounds__(256) scan_step_quad_kernel(StepParams p, int64
     y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
     y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
     y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (FUSED) {
+      const int64_t c0 = i0 >> 2, c1 = i1 >> 2;
+      if (live0 && q == 0) y0 = step_output<T>(p, y0, v0.xv, c0, static_cast<uint32_t>(c0) % static_cast<uint32_t>(p.D));
+      if (live1 && q == 0) y1 = step_output<T>(p, y1, v1.xv, c1, static_cast<uint32_t>(c1) % static_cast<uint32_t>(p.D));
+    }
     if (live0 && q == 0) Elem<T>::store(p.y, i0 >> 2, y0);
     if (live1 && q == 0) Elem<T>::store(p.y, i1 >> 2, y1);
   }
@@ -124,7 +148,7 @@ __global__ void __launch_bounds__(256) scan_step_kernel(StepParams p) {
   const int N = static_cast<int>(p.N);
   const int64_t b = i / p.D, d = i % p.D;
   const float xv = Elem<T>::load(p.x, i);
-  const float dt = Elem<T>::load(p.delta, i);
+  const float dt = step_delta(p, Elem<T>::load(p.delta, i), d);
   float h[NP];
   float* srow = p.state + i * N;
   if (VEC) {
@@ -164,7 +188,7 @@ __global__ void __launch_bounds__(256) scan_step_kernel(StepParams p) {
     for (int n = 0; n < NP; ++n)
       if (n < N) srow[n] = h[n];
   }
-  Elem<T>::store(p.y, i, yv);
+  Elem<T>::store(p.y, i, step_output<T>(p, yv, xv, i, d));
 }
 
 template <int NP, bool ZOH, typename T, bool VEC>
@@ -185,7 +209,10 @@ cudaError_t pick(const StepParams& sp, cudaStream_t s) {
     const int64_t cap = static_cast<int64_t>(sm_count()) * 8;  // persistent: 8 resident 256-thread blocks per SM
     blocks = (blocks + 1) / 2;                                   // two items per lane per trip
     if (blocks > cap) blocks = cap;
-    scan_step_quad_kernel<ZOH, T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(sp, quads);
+    if (sp.delta_bias || sp.softplus || sp.D_skip || sp.z)
+      scan_step_quad_kernel<ZOH, true, T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(sp, quads);
+    else
+      scan_step_quad_kernel<ZOH, false, T><<<static_cast<unsigned>(blocks), 256, 0, s>>>(sp, quads);
     return cudaGetLastError();
   }
   if (sp.N == 16 && aligned) return go<16, ZOH, T, true>(sp, s);
@@ -199,7 +226,8 @@ cudaError_t pick(const StepParams& sp, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_step(const StepArgs& a) {
-  StepParams sp{a.state, a.x, a.delta, a.A_log, a.B, a.C, a.y, a.batch, a.D, a.N};
+  StepParams sp{a.state, a.x, a.delta, a.A_log, a.B, a.C, a.y, a.batch, a.D, a.N,
+                a.delta_bias, a.softplus, a.D_skip, a.z};
   if (a.disc == 1)
     return a.dtype == 1 ? pick<true, __nv_bfloat16>(sp, a.stream) : pick<true, float>(sp, a.stream);
   return a.dtype == 1 ? pick<false, __nv_bfloat16>(sp, a.stream) : pick<false, float>(sp, a.stream);

@@ -1,0 +1,158 @@
+"""Parity of the fused layer pieces (softplus(delta + bias), + D x, * SiLU(z)) on the CUDA path, through the
+C ABI, with the fp64 oracle given the same pieces."""
+import math
+
+import numpy as np
+import pytest
+
+import ssm_inputs
+from gpu_util import dev_inputs, host_values
+from tolerance import TOL, rel_err
+
+pytestmark = pytest.mark.gpu
+
+COMBOS = {
+    # name: (delta_softplus, with bias, with D_skip, with z); the first three run on the TMA path (N = 16)
+    "softplus_bias_skip_gate": (True, True, True, True),
+    "softplus_bias_skip": (True, True, True, False),
+    "softplus_only": (True, False, False, False),
+    "skip_only": (False, False, True, False),
+    "gate_only": (False, False, False, True),
+    "bias_no_softplus": (False, True, False, False),
+}
+
+
+def _pieces(rng, batch, L, D, combo, dtype):
+    sp, with_bias, with_skip, with_z = combo
+    # without the softplus the bias is added to an already positive delta: keep it non-negative, so that the
+    # step stays a step (a negative delta grows the state without bound over long sequences)
+    lo = -1.0 if sp else 0.0
+    bias = rng.uniform(lo, 1.0, D).astype(np.float32) if with_bias else None
+    dskip = rng.standard_normal(D).astype(np.float32) if with_skip else None
+    z = rng.standard_normal((batch, L, D)).astype(np.float32) if with_z else None
+    if z is not None and dtype == "bf16":
+        z = ssm_inputs.bf16_to_f32(ssm_inputs.bf16_round(z)).reshape(z.shape)
+    return sp, bias, dskip, z
+
+
+def _dev(a, dtype):
+    import torch
+    if a is None:
+        return None
+    if dtype == "bf16":
+        return torch.from_numpy(ssm_inputs.bf16_round(a).view(np.int16).copy()).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+
+
+def _f32(a):
+    import torch
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+
+
+SHAPES = [(2, 500, 128, 16), (1, 3000, 64, 16), (1, 300, 70, 8)]  # TMA path x2, general path
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"b{s[0]}_L{s[1]}_D{s[2]}_N{s[3]}" for s in SHAPES])
+@pytest.mark.parametrize("combo", sorted(COMBOS))
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fwd_fused(orc, shape, combo, disc, dtype):
+    import selective_state_space_124_b300 as lib
+    batch, L, D, N = shape
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=7 * L + D, dtype=dtype)
+    rng = np.random.default_rng(L + D)
+    # raw delta (before softplus) for the combos that apply it inside the scan
+    sp, bias, dskip, z = _pieces(rng, batch, L, D, COMBOS[combo], dtype)
+    if sp:
+        raw = rng.normal(-2.5, 1.0, (batch, L, D)).astype(np.float32)
+        inp["delta"] = raw
+        inp.pop("delta_bits", None)
+    d = dev_inputs(inp, dtype)
+    y, fs = lib.ssm_scan_fwd(d["x"], d["delta"], d["A_log"], d["B"], d["C"], disc=disc, delta_bias=_f32(bias),
+                             delta_softplus=sp, D_skip=_f32(dskip), z=_dev(z, dtype))
+    lib.check_device()
+    hv = host_values(inp, dtype)
+    yr, sr = orc.scan_fwd(hv["x"], hv["delta"], inp["A_log"], hv["B"], hv["C"], disc=disc, delta_bias=bias,
+                          delta_softplus=sp, D_skip=dskip, z=z)
+    ey = rel_err(y.float().cpu().numpy(), yr)
+    es = rel_err(fs.cpu().numpy(), sr)
+    assert ey <= TOL[dtype], f"y rel err {ey:.3g}"
+    assert es <= TOL[dtype], f"final state rel err {es:.3g}"
+
+
+@pytest.mark.parametrize("D", [1, 64])  # general path (N = 1) and, with 16 entries, the TMA path
+def test_page_trace_with_softplus_inside(orc, D):
+    """The chapter's trace Delta_t = softplus(x_t - 5), formed by the kernel from raw x_t and bias -5, in
+    every channel; N = 1 (general kernel) or N = 16 with B = e_0, C = e_0 (TMA kernel)."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    from golden_io import load
+    g = load("euler_scalar_trace.txt")
+    xs = np.asarray(g["x"], np.float32)
+    L, N = len(xs), (1 if D == 1 else 16)
+    x = torch.from_numpy(np.repeat(xs.reshape(1, L, 1), D, axis=2).copy()).cuda()
+    onehot = np.zeros((1, L, N), np.float32)
+    onehot[..., 0] = 1.0
+    A_log = np.zeros((D, N), np.float32)
+    A_log[:, 1:] = np.log(np.arange(2, N + 1))  # A_n = -(n + 1): the structured form, entry 0 is the trace
+    Bt = torch.from_numpy(onehot).cuda()
+    y, _ = lib.ssm_scan_fwd(x, x, torch.from_numpy(A_log).cuda(), Bt, Bt, disc="euler",
+                            delta_bias=torch.full((D,), float(g["bias"][0]), device="cuda"), delta_softplus=True)
+    lib.check_device()
+    got = y.cpu().numpy()[0]
+    for d in range(D):
+        assert np.max(np.abs(got[:, d] - np.asarray(g["h"])) / np.asarray(g["h"])) < 3e-6
+
+
+@pytest.mark.parametrize("shape", [(4, 257, 16), (3, 70, 8)])  # four-lanes-per-channel kernel, general kernel
+@pytest.mark.parametrize("combo", sorted(COMBOS))
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_step_fused(orc, shape, combo, disc, dtype):
+    import torch
+    import selective_state_space_124_b300 as lib
+    batch, D, N = shape
+    rng = np.random.default_rng(batch * 100 + D)
+    sp, bias, dskip, z = _pieces(rng, batch, 1, D, COMBOS[combo], dtype)
+    z = None if z is None else z.reshape(batch, D)
+    st = rng.standard_normal((batch, D, N)).astype(np.float32)
+    x = rng.standard_normal((batch, D)).astype(np.float32)
+    dt = (rng.normal(-2.5, 1.0, (batch, D)) if sp else np.log1p(np.exp(rng.normal(-2, 1, (batch, D))))).astype(np.float32)
+    B = rng.standard_normal((batch, N)).astype(np.float32)
+    C = rng.standard_normal((batch, N)).astype(np.float32)
+    A_log = ssm_inputs.a_log_s4d(D, N)
+    vals = {k: (ssm_inputs.bf16_to_f32(ssm_inputs.bf16_round(a)).reshape(a.shape) if dtype == "bf16" else a)
+            for k, a in (("x", x), ("dt", dt), ("B", B), ("C", C))}
+    state = torch.from_numpy(st).cuda()
+    y = lib.ssm_scan_step(state, _dev(x, dtype), _dev(dt, dtype), torch.from_numpy(A_log).cuda(), _dev(B, dtype),
+                          _dev(C, dtype), disc=disc, delta_bias=_f32(bias), delta_softplus=sp, D_skip=_f32(dskip),
+                          z_t=_dev(z, dtype))
+    lib.check_device()
+    sr, yr = orc.scan_step(st.astype(np.float64), vals["x"], vals["dt"], A_log, vals["B"], vals["C"], disc=disc,
+                           delta_bias=bias, delta_softplus=sp, D_skip=dskip, z_t=z)
+    assert rel_err(y.float().cpu().numpy(), yr) <= TOL[dtype]
+    assert rel_err(state.cpu().numpy(), sr) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_fused_prefill_then_steps_matches_one_prefill(disc):
+    """Prefill over [0, k) then fused decode steps over [k, L) equal one fused prefill over [0, L)."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    batch, L, D, N, k = 2, 96, 128, 16, 60
+    rng = np.random.default_rng(5)
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=61)
+    inp["delta"] = rng.normal(-2.5, 1.0, (batch, L, D)).astype(np.float32)
+    d = dev_inputs(inp, "f32")
+    bias, dskip = _f32(rng.uniform(-1, 1, D)), _f32(rng.standard_normal(D))
+    z = _f32(rng.standard_normal((batch, L, D)))
+    kw = dict(disc=disc, delta_bias=bias, delta_softplus=True, D_skip=dskip)
+    y, fs = lib.ssm_scan_fwd(d["x"], d["delta"], d["A_log"], d["B"], d["C"], z=z, **kw)
+    sl = lambda t, a, b_: t[:, a:b_].contiguous()
+    _, state = lib.ssm_scan_fwd(sl(d["x"], 0, k), sl(d["delta"], 0, k), d["A_log"], sl(d["B"], 0, k),
+                                sl(d["C"], 0, k), z=sl(z, 0, k), **kw)
+    for t in range(k, L):
+        yt = lib.ssm_scan_step(state, d["x"][:, t].contiguous(), d["delta"][:, t].contiguous(), d["A_log"],
+                               d["B"][:, t].contiguous(), d["C"][:, t].contiguous(), z_t=z[:, t].contiguous(), **kw)
+        assert rel_err(yt.cpu().numpy(), y[:, t].cpu().numpy()) <= 1e-5
+    assert rel_err(state.cpu().numpy(), fs.cpu().numpy()) <= 1e-5
