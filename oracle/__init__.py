@@ -16,7 +16,10 @@ Three independent evaluations of the same function live here:
 * ``lti_conv`` -- the convolution view of a time-invariant system ("Understanding Mamba" s3.1,
   Eqs. (4)-(5)): taps K_i = C . Abar^i . Bbar, y = x * K, through ``numpy.convolve``.
 
-All three run in float64. Discretisation names: ``"euler"`` (Bbar = delta * B, Abar kept exact) and
+``Oracle.scan_bwd`` gives the gradients of the prefill scan by the adjoint recurrence run backwards in
+time (``ssm_oracle.c``); the tests pin it to central finite differences of ``scan_fwd``.
+
+All of them run in float64. Discretisation names: ``"euler"`` (Bbar = delta * B, Abar kept exact) and
 ``"zoh"`` (Bbar = (exp(delta A) - 1) / A * B).
 """
 from __future__ import annotations
@@ -68,6 +71,9 @@ class Oracle:
         lib.oracle_scan_step_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i64, i64, i64, i32, i32, vp,
                                             i64, vp]
         lib.oracle_scan_step_ex.restype = i32
+        lib.oracle_scan_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, vp, i64,
+                                        vp, vp, vp, vp, vp, vp]
+        lib.oracle_scan_bwd.restype = i32
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         self.lib = lib
@@ -154,6 +160,53 @@ class Oracle:
         return st, y
 
 
+    def scan_bwd(self, x, delta, A_log, B, C, dy, disc="euler", h0=None, dfinal=None, channels=None, f64=None,
+                 want_bc=True):
+        """Gradients of the prefill scan (see ssm_oracle.c, oracle_scan_bwd) for the objective
+        sum(dy * y) + sum(dfinal * final_state). dy has x's shape; h0 and dfinal are indexed like
+        final_state (optional, zero when None).
+
+        Returns a dict of float64 arrays. With ``channels`` None: dx, ddelta [batch, L, D];
+        dA_log [D, N] (summed over the batch); dB, dC [batch, L, N] (summed over channels); dh0
+        [batch, D, N]. With a channel list: dx, ddelta [n_chan, L]; dA_log [n_chan, N] (each listed
+        channel's own contribution); dB, dC [n_chan, L, N] per channel when ``want_bc``, else None;
+        dh0 [n_chan, N].
+        """
+        arrs = [np.asarray(a) for a in (x, delta, A_log, B, C, dy)]
+        if f64 is None:
+            f64 = any(a.dtype == np.float64 for a in arrs)
+        x, delta, A_log, B, C, dy = (_as_input(a, f64) for a in arrs)
+        batch, L, D = x.shape
+        N = A_log.shape[1]
+        assert delta.shape == x.shape and dy.shape == x.shape and A_log.shape == (D, N)
+        assert B.shape == (batch, L, N) and C.shape == (batch, L, N)
+        chan = None if channels is None else np.ascontiguousarray(channels, dtype=np.int64)
+        n_chan = batch * D if chan is None else len(chan)
+
+        def per_chan(a):
+            return None if a is None else np.ascontiguousarray(np.asarray(a, np.float64).reshape(n_chan, N))
+        h0c, dfc = per_chan(h0), per_chan(dfinal)
+        bc = want_bc or chan is None
+        dx = np.empty((n_chan, L)); ddt = np.empty((n_chan, L)); dal = np.empty((n_chan, N))
+        dB = np.empty((n_chan, L, N)) if bc else None
+        dC = np.empty((n_chan, L, N)) if bc else None
+        dh0 = np.empty((n_chan, N))
+        rc = self.lib.oracle_scan_bwd(
+            x.ctypes.data, delta.ctypes.data, A_log.ctypes.data, B.ctypes.data, C.ctypes.data,
+            None if h0c is None else h0c.ctypes.data, dy.ctypes.data, None if dfc is None else dfc.ctypes.data,
+            batch, L, D, N, DISC[disc], int(f64), None if chan is None else chan.ctypes.data, n_chan,
+            dx.ctypes.data, ddt.ctypes.data, dal.ctypes.data, None if dB is None else dB.ctypes.data,
+            None if dC is None else dC.ctypes.data, dh0.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_scan_bwd rejected its arguments")
+        if chan is not None:
+            return {"dx": dx, "ddelta": ddt, "dA_log": dal, "dB": dB, "dC": dC, "dh0": dh0}
+        per = lambda a: a.reshape(batch, D, L).transpose(0, 2, 1).copy()
+        return {"dx": per(dx), "ddelta": per(ddt), "dA_log": dal.reshape(batch, D, N).sum(axis=0),
+                "dB": dB.reshape(batch, D, L, N).sum(axis=1), "dC": dC.reshape(batch, D, L, N).sum(axis=1),
+                "dh0": dh0.reshape(batch, D, N)}
+
+
 _default: Oracle | None = None
 
 
@@ -170,6 +223,10 @@ def scan_fwd(*args, **kw):
 
 def scan_step(*args, **kw):
     return default().scan_step(*args, **kw)
+
+
+def scan_bwd(*args, **kw):
+    return default().scan_bwd(*args, **kw)
 
 
 def num_threads() -> int:

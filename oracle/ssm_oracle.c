@@ -46,6 +46,7 @@
  * Parallelism: OpenMP over independent channels only; each channel is one sequential loop.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stddef.h>
 #include <stdint.h>
 #ifdef _OPENMP
@@ -196,4 +197,129 @@ int oracle_scan_step(double *state, const void *x_t, const void *delta_t, const 
 {
     return oracle_scan_step_ex(state, x_t, delta_t, A_log, B_t, C_t, 0, 0, 0, 0, batch, D, N, disc, is_f64, chan,
                                n_chan, y_t);
+}
+
+/*
+ * ---- Backward pass (gradients of the prefill scan) ---------------------------------------------------
+ *
+ * The pages say only that the backward pass recomputes the states h instead of storing them ("State
+ * Space Models & Mamba" chapter, the paragraph on the fused kernel). What it must produce is fixed by
+ * the forward definition above: the gradients of
+ *     J = sum_{b,t,d} dy[b,t,d] * y[b,t,d] + sum_{b,d,n} dfinal[b,d,n] * final_state[b,d,n]
+ * with respect to x, delta, A_log, B, C and h0, for the plain scan (no softplus, feedthrough or gate).
+ * This oracle keeps every h_t of the channel (it is the plain reading, not the memory-saving one) and runs
+ * the adjoint recurrence of h_t = abar_t h_{t-1} + bbar_t x_t backwards in time:
+ *     lambda_t = C_t dy_t + abar_{t+1} lambda_{t+1},    lambda_{L-1} = C_{L-1} dy_{L-1} + dfinal
+ * (lambda_t = dJ/dh_t), and for every step and entry
+ *     dx_t     += lambda_t bbar_t                 (bbar_t = delta_t B_t (Euler) or expm1(delta_t A)/A B_t)
+ *     d abar_t  = lambda_t h_{t-1}                d bbar_t = lambda_t x_t
+ *     dC_t     += dy_t h_t
+ *     ddelta_t += d abar_t A abar_t + d bbar_t (Euler: B_t; ZOH: abar_t B_t)
+ *     dA       += d abar_t delta_t abar_t + (ZOH only) d bbar_t B_t delta_t^2 f(delta_t A)
+ *     dB_t     += d bbar_t (Euler: delta_t; ZOH: expm1(delta_t A)/A)
+ * where f(w) = (w e^w - expm1(w)) / w^2 is d/dA [expm1(delta A)/A] / delta^2 (limit 1/2 at A = 0, the
+ * same continuous extension the forward uses for bbar there), and finally dh0 = abar_0 lambda_0 and
+ * dA_log = dA * A (A = -exp(A_log)).
+ */
+
+/* f(w) = (w e^w - expm1(w)) / w^2, with its Taylor series 1/2 + w/3 + w^2/8 + w^3/30 near 0 where the
+   difference cancels. */
+static double oracle_zoh_dA_factor(double w)
+{
+    if (fabs(w) < 1e-3) return 0.5 + w * (1.0 / 3.0 + w * (1.0 / 8.0 + w / 30.0));
+    return (w * exp(w) - expm1(w)) / (w * w);
+}
+
+/* bbar / B for one entry: delta (Euler), expm1(delta A)/A (ZOH; delta where A == 0). */
+static double oracle_bfac(double dlt, double a_n, int disc)
+{
+    if (disc == ORACLE_ZOH && a_n != 0.0) return expm1(dlt * a_n) / a_n;
+    return dlt;
+}
+
+/*
+ * Gradients for the listed channels (chan as in oracle_scan_fwd_ex). Per listed channel k:
+ *   dx_out[k*L + t], ddelta_out[k*L + t]      gradients of that channel's x and delta
+ *   dA_log_out[k*N + n]                        that channel's contribution to dA_log[d, n] (the caller
+ *                                              sums the contributions of the batch elements)
+ *   dB_out[(k*L + t)*N + n], dC_out[...]       that channel's contribution to dB[b,t,n], dC[b,t,n]
+ *                                              (the caller sums over d); either may be NULL
+ *   dh0_out[k*N + n]                           dJ/dh0 (NULL: not wanted)
+ * dy: [batch, L, D] like x; dfinal, h0: [n_chan, N] doubles or NULL (zero).
+ */
+int oracle_scan_bwd(const void *x, const void *delta, const void *A_log, const void *B, const void *C,
+                    const double *h0, const void *dy, const double *dfinal,
+                    int64_t batch, int64_t L, int64_t D, int64_t N, int disc, int is_f64,
+                    const int64_t *chan, int64_t n_chan,
+                    double *dx_out, double *ddelta_out, double *dA_log_out, double *dB_out, double *dC_out,
+                    double *dh0_out)
+{
+    if (batch < 0 || L < 0 || D < 0 || N < 1 || N > ORACLE_MAX_N) return -1;
+    if (disc != ORACLE_EULER && disc != ORACLE_ZOH) return -1;
+    int64_t total = chan ? n_chan : batch * D;
+    int bad = 0;
+#pragma omp parallel reduction(| : bad)
+    {
+        double *H = (double *)malloc((size_t)(L > 0 ? L : 1) * (size_t)N * sizeof(double));  /* h_t, t < L */
+        if (!H) bad = 1;
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t k = 0; k < total; ++k) {
+            int64_t flat = chan ? chan[k] : k;
+            if (!H || flat < 0 || flat >= batch * D) { bad = 1; continue; }
+            int64_t b = flat / D, d = flat % D;
+            double A[ORACLE_MAX_N], h[ORACLE_MAX_N], lam[ORACLE_MAX_N], mu[ORACLE_MAX_N], dA[ORACLE_MAX_N];
+            for (int64_t n = 0; n < N; ++n) {
+                A[n] = -exp(ld(A_log, d * N + n, is_f64));
+                h[n] = h0 ? h0[k * N + n] : 0.0;
+                mu[n] = dfinal ? dfinal[k * N + n] : 0.0;   /* dJ/dh_{L-1} from the final state */
+                dA[n] = 0.0;
+            }
+            /* forward, keeping every state */
+            for (int64_t t = 0; t < L; ++t) {
+                double xt = ld(x, (b * L + t) * D + d, is_f64);
+                double dt = ld(delta, (b * L + t) * D + d, is_f64);
+                for (int64_t n = 0; n < N; ++n) {
+                    h[n] = exp(dt * A[n]) * h[n] + oracle_bfac(dt, A[n], disc) * ld(B, (b * L + t) * N + n, is_f64) * xt;
+                    H[t * N + n] = h[n];
+                }
+            }
+            /* backward */
+            for (int64_t t = L - 1; t >= 0; --t) {
+                double xt = ld(x, (b * L + t) * D + d, is_f64);
+                double dt = ld(delta, (b * L + t) * D + d, is_f64);
+                double dyt = ld(dy, (b * L + t) * D + d, is_f64);
+                double gx = 0.0, gdt = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    int64_t bc = (b * L + t) * N + n;
+                    double Bn = ld(B, bc, is_f64), Cn = ld(C, bc, is_f64);
+                    double abar = exp(dt * A[n]);
+                    double bfac = oracle_bfac(dt, A[n], disc);
+                    double hprev = t > 0 ? H[(t - 1) * N + n] : (h0 ? h0[k * N + n] : 0.0);
+                    lam[n] = Cn * dyt + mu[n];
+                    double g_abar = lam[n] * hprev;
+                    double g_bbar = lam[n] * xt;          /* gradient of bbar = bfac * B */
+                    gx += lam[n] * bfac * Bn;
+                    gdt += g_abar * A[n] * abar;
+                    dA[n] += g_abar * dt * abar;
+                    if (disc == ORACLE_ZOH) {
+                        gdt += g_bbar * abar * Bn;
+                        dA[n] += g_bbar * Bn * dt * dt * oracle_zoh_dA_factor(dt * A[n]);
+                    } else {
+                        gdt += g_bbar * Bn;
+                    }
+                    if (dB_out) dB_out[(k * L + t) * N + n] = g_bbar * bfac;
+                    if (dC_out) dC_out[(k * L + t) * N + n] = dyt * H[t * N + n];
+                    mu[n] = abar * lam[n];
+                }
+                dx_out[k * L + t] = gx;
+                ddelta_out[k * L + t] = gdt;
+            }
+            for (int64_t n = 0; n < N; ++n) {
+                dA_log_out[k * N + n] = dA[n] * A[n];
+                if (dh0_out) dh0_out[k * N + n] = mu[n];
+            }
+        }
+        free(H);
+    }
+    return bad ? -1 : 0;
 }

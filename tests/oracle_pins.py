@@ -393,9 +393,116 @@ def pin_feedthrough_and_gate(orc):
         _close(y[0, :, 0], base[0, :, 0] * want, 1e-12 * max(1.0, abs(want)), f"gate at z = {zv}")
 
 
+# --- backward pass (gradients of the prefill scan) -------------------------------------------------------
+# The pages fix only that the backward pass recomputes h ("State Space Models & Mamba" chapter, the fused-
+# kernel paragraph); the gradients themselves are fixed by the forward definition, so they are pinned to
+# central finite differences of the forward oracle, to the adjoint of the convolution view, and to closed
+# forms of one step.
+
+def _bwd_problem(rng, batch, L, D, N, A_lo, A_hi, dt_lo, dt_hi):
+    x = rng.standard_normal((batch, L, D))
+    dt = rng.uniform(dt_lo, dt_hi, (batch, L, D))
+    A_log = np.log(rng.uniform(A_lo, A_hi, (D, N)))
+    B = rng.standard_normal((batch, L, N))
+    C = rng.standard_normal((batch, L, N))
+    dy = rng.standard_normal((batch, L, D))
+    h0 = rng.standard_normal((batch, D, N))
+    dfinal = rng.standard_normal((batch, D, N))
+    return x, dt, A_log, B, C, dy, h0, dfinal
+
+
+def _fd_check(orc, disc, x, dt, A_log, B, C, dy, h0, dfinal, tol, what):
+    g = orc.scan_bwd(x, dt, A_log, B, C, dy, disc=disc, h0=h0, dfinal=dfinal, f64=True)
+    inputs = {"x": x, "dt": dt, "A_log": A_log, "B": B, "C": C, "h0": h0}
+
+    def J(vals):
+        y, f = orc.scan_fwd(vals["x"], vals["dt"], vals["A_log"], vals["B"], vals["C"], disc=disc, h0=vals["h0"],
+                            f64=True)
+        return float(np.sum(y * dy) + np.sum(f * dfinal))
+    for name, key in (("x", "dx"), ("dt", "ddelta"), ("A_log", "dA_log"), ("B", "dB"), ("C", "dC"), ("h0", "dh0")):
+        arr = inputs[name]
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            eps = 1e-6 * max(1.0, abs(arr[idx]))
+            vals = dict(inputs)
+            p = arr.copy(); p[idx] += eps
+            m = arr.copy(); m[idx] -= eps
+            vals[name] = p; jp = J(vals)
+            vals[name] = m; jm = J(vals)
+            fd[idx] = (jp - jm) / (2.0 * eps)
+        scale = max(np.abs(fd).max(), 1e-300)
+        _close(g[key], fd, tol * scale, f"{what}: {key} vs central differences ({disc})")
+
+
+def pin_bwd_finite_differences(orc):
+    """Every gradient equals the central difference of sum(dy y) + sum(dfinal final_state) computed with the
+    forward oracle, both discretisations, with an initial state; a second case keeps |delta A| below 1e-3,
+    where the ZOH gradient in A goes through its small-argument series."""
+    rng = np.random.default_rng(21)
+    for disc in ("euler", "zoh"):
+        _fd_check(orc, disc, *_bwd_problem(rng, 2, 6, 2, 3, 0.3, 3.0, 0.05, 0.7), 1e-7, "random")
+    _fd_check(orc, "zoh", *_bwd_problem(rng, 1, 5, 2, 3, 1e-3, 1e-2, 0.01, 0.1), 1e-6, "small delta A")
+
+
+def pin_bwd_convolution_adjoint(orc):
+    """Time-invariant case (fixed delta, B, C; zero initial state): y = x * K ("Understanding Mamba" s3.1), so
+    dJ/dx_j = sum_{t >= j} dy_t K_{t-j}, the correlation of dy with the kernel's taps."""
+    rng = np.random.default_rng(22)
+    L, N = 12, 3
+    A_log = rng.uniform(-1.0, 1.0, N)
+    Bv, Cv = rng.standard_normal(N), rng.standard_normal(N)
+    x, dy = rng.standard_normal(L), rng.standard_normal(L)
+    for disc in ("euler", "zoh"):
+        _, K = oracle_mod.lti_conv(x, 0.4, A_log, Bv, Cv, disc=disc)
+        want = np.array([np.sum(dy[j:] * K[:L - j]) for j in range(L)])
+        g = orc.scan_bwd(_chan1(x), _chan1(np.full(L, 0.4)), A_log.reshape(1, N), np.tile(Bv, (1, L, 1)),
+                         np.tile(Cv, (1, L, 1)), _chan1(dy), disc=disc, f64=True)
+        _close(g["dx"][0, :, 0], want, 1e-12 * np.abs(want).max(), f"dx as the correlation with K ({disc})")
+
+
+def pin_bwd_one_step(orc):
+    """One step, one entry, by hand: h = a h0 + bf B x, y = C h, J = dy y + df h, lambda = C dy + df:
+    dx = lambda bf B, dh0 = lambda a, dC = dy h, dB = lambda bf x, and
+    ddelta = lambda (A a h0 + B x) (Euler, bf = delta) or lambda (A a h0 + a B x) (ZOH, bf = (a - 1)/A)."""
+    x, dt, A, h0, Bv, Cv, dy, df = 0.7, 0.3, -1.5, 0.4, 1.2, -0.8, 0.9, 0.25
+    a = math.exp(dt * A)
+    lam = Cv * dy + df
+    for disc, bf, dd, dA in (
+            ("euler", dt, lam * (A * a * h0 + Bv * x), lam * h0 * dt * a),
+            ("zoh", (a - 1.0) / A, lam * (A * a * h0 + a * Bv * x),
+             lam * h0 * dt * a + lam * x * Bv * (dt * A * a - (a - 1.0)) / (A * A))):
+        h = a * h0 + bf * Bv * x
+        g = orc.scan_bwd(_chan1([x]), _chan1([dt]), np.full((1, 1), math.log(-A)), _bc([[Bv]]), _bc([[Cv]]),
+                         _chan1([dy]), disc=disc, h0=np.full((1, 1, 1), h0), dfinal=np.full((1, 1, 1), df), f64=True)
+        for key, want in (("dx", lam * bf * Bv), ("dh0", lam * a), ("dC", dy * h), ("dB", lam * bf * x),
+                          ("ddelta", dd), ("dA_log", dA * A)):
+            _close(np.ravel(g[key])[0], want, 1e-14, f"one step {key} ({disc})")
+
+
+def pin_bwd_split(orc):
+    """Reverse-time associativity: the gradients over [0, L) equal those of [k, L) (started from the state at
+    k) followed by those of [0, k) with dfinal = the second half's dJ/dh0; dA_log and the per-step gradients
+    add up piecewise."""
+    rng = np.random.default_rng(23)
+    x, dt, A_log, B, C, dy, h0, dfinal = _bwd_problem(rng, 2, 20, 3, 4, 0.3, 3.0, 0.05, 0.7)
+    k = 8
+    for disc in ("euler", "zoh"):
+        g = orc.scan_bwd(x, dt, A_log, B, C, dy, disc=disc, h0=h0, dfinal=dfinal, f64=True)
+        _, s1 = orc.scan_fwd(x[:, :k], dt[:, :k], A_log, B[:, :k], C[:, :k], disc=disc, h0=h0, f64=True)
+        g2 = orc.scan_bwd(x[:, k:], dt[:, k:], A_log, B[:, k:], C[:, k:], dy[:, k:], disc=disc, h0=s1,
+                          dfinal=dfinal, f64=True)
+        g1 = orc.scan_bwd(x[:, :k], dt[:, :k], A_log, B[:, :k], C[:, :k], dy[:, :k], disc=disc, h0=h0,
+                          dfinal=g2["dh0"], f64=True)
+        for key in ("dx", "ddelta", "dB", "dC"):
+            _close(np.concatenate([g1[key], g2[key]], 1), g[key], 1e-12, f"split {key} ({disc})")
+        _close(g1["dA_log"] + g2["dA_log"], g["dA_log"], 1e-12, f"split dA_log ({disc})")
+        _close(g1["dh0"], g["dh0"], 1e-12, f"split dh0 ({disc})")
+
+
 ALL_PINS = [
     pin_leaky_bucket_closed_form, pin_ema_identity, pin_euler_scalar_trace, pin_active_recall_traces,
     pin_lti_zoh_example, pin_convolution_view, pin_selective_zoh_example, pin_combine_tree,
     pin_small_delta_limit, pin_unit_input_two_step, pin_delta_limits, pin_brute_force_1ss,
-    pin_split_and_step, pin_softplus_inside_scan, pin_feedthrough_and_gate,
+    pin_split_and_step, pin_softplus_inside_scan, pin_feedthrough_and_gate, pin_bwd_finite_differences,
+    pin_bwd_convolution_adjoint, pin_bwd_one_step, pin_bwd_split,
 ]

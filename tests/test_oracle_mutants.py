@@ -42,6 +42,18 @@ MUTANTS = {
     "skip_dropped": ("double out = yssm + (dskip ? dskip[d] * x : 0.0);", "double out = yssm;"),
     "gate_sigmoid_not_silu": ("out *= zv / (1.0 + exp(-zv));", "out *= 1.0 / (1.0 + exp(-zv));"),
     "gate_sign_flipped": ("out *= zv / (1.0 + exp(-zv));", "out *= zv / (1.0 + exp(zv));"),
+    "bwd_hprev_is_h": ("double hprev = t > 0 ? H[(t - 1) * N + n]", "double hprev = t > 0 ? H[t * N + n]"),
+    "bwd_adjoint_without_decay": ("mu[n] = abar * lam[n];", "mu[n] = lam[n];"),
+    "bwd_zoh_dA_term_dropped": ("dA[n] += g_bbar * Bn * dt * dt * oracle_zoh_dA_factor(dt * A[n]);", ""),
+    "bwd_zoh_series_wrong": ("0.5 + w * (1.0 / 3.0", "0.5 + w * (1.0 / 2.0"),
+    "bwd_euler_ddelta_input_term": ("gdt += g_bbar * Bn;", ""),
+    "bwd_zoh_ddelta_without_abar": ("gdt += g_bbar * abar * Bn;", "gdt += g_bbar * Bn;"),
+    "bwd_dA_log_chain_sign": ("dA_log_out[k * N + n] = dA[n] * A[n];", "dA_log_out[k * N + n] = -dA[n] * A[n];"),
+    "bwd_dfinal_ignored": ("mu[n] = dfinal ? dfinal[k * N + n] : 0.0;", "mu[n] = 0.0;"),
+    "bwd_dC_uses_previous_state": ("dC_out[(k * L + t) * N + n] = dyt * H[t * N + n];",
+                                   "dC_out[(k * L + t) * N + n] = dyt * hprev;"),
+    "bwd_dx_missing_B": ("gx += lam[n] * bfac * Bn;", "gx += lam[n] * bfac;"),
+    "bwd_dh0_undecayed": ("if (dh0_out) dh0_out[k * N + n] = mu[n];", "if (dh0_out) dh0_out[k * N + n] = lam[n];"),
     "channel_index_swapped": ("int64_t b = flat / D, d = flat % D;\n        double h[",
                               "int64_t d = flat / D, b = flat % D;\n        double h["),
 }
