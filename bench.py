@@ -78,6 +78,15 @@ def fwd_bytes(cfg):
     return 3 * b * L * D * es + 2 * b * L * N * es + D * N * 4 + b * D * N * 4
 
 
+def bwd_bytes(cfg):
+    """Compulsory bytes of one backward launch: x, delta, dy, B, C, A_log read; dx, ddelta (input dtype) and
+    dA_log, dB, dC, dh0 (fp32) written. The recomputed states and the workspace's chunk-end states are not
+    counted."""
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    b, L, D, N = cfg["batch"], cfg["L"], cfg["D"], cfg["N"]
+    return 5 * b * L * D * es + 2 * b * L * N * es + 2 * b * L * N * 4 + 2 * D * N * 4 + b * D * N * 4
+
+
 def step_bytes(cfg):
     """Compulsory bytes of one decode step: state read + written, x_t, delta_t, y_t, B_t, C_t, A_log."""
     es = 2 if cfg["dtype"] == "bf16" else 4
@@ -273,6 +282,52 @@ def measure_prefill(name, reps, flush, peak, fused=False):
     what = describe(name, cfg).split(";")[0] + ("; fused softplus(delta + bias), + D x, * SiLU(z)" if fused else "")
     return {"workload": what, "launch_ms_median": med * 1e3, "elems_per_s": b * L * D / med, "gbs": gbs,
             "hbm_frac": gbs / peak, "bytes_per_launch": nbytes, "reps": reps}
+
+
+def measure_backward(name, reps, flush, peak):
+    """Backward pass of a prefill workload (ssm_scan_bwd through the C ABI, dy ~ N(0, 1), no initial state,
+    no final-state gradient), timed like the prefill: L2 flushed before each launch, CUDA events."""
+    import ctypes
+    import torch
+    import selective_state_space_124_b300 as lib
+    from selective_state_space_124_b300 import _ffi
+    cfg = dict(ssm_inputs.WORKLOADS[name])
+    inp = ssm_inputs.workload_inputs(name)
+    bf16 = cfg["dtype"] == "bf16"
+    b, L, D, N = cfg["batch"], cfg["L"], cfg["D"], cfg["N"]
+    inp["dy"] = np.random.default_rng(5).standard_normal((b, L, D)).astype(np.float32)
+    d = {k: _dev_tensor(torch, inp[k], bf16) for k in ("x", "delta", "B", "C", "dy")}
+    A = torch.from_numpy(inp["A_log"].copy()).cuda()
+    tdt = torch.bfloat16 if bf16 else torch.float32
+    out = [torch.empty((b, L, D), dtype=tdt, device="cuda"), torch.empty((b, L, D), dtype=tdt, device="cuda"),
+           torch.empty((D, N), device="cuda"), torch.empty((b, L, N), device="cuda"),
+           torch.empty((b, L, N), device="cuda"), torch.empty((b, D, N), device="cuda")]
+    need = lib.bwd_workspace_size(b, L, D, N)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    v = ctypes.c_void_p
+    fn = _ffi.load().ssm_scan_bwd
+    cargs = (v(d["x"].data_ptr()), v(d["delta"].data_ptr()), v(A.data_ptr()), v(d["B"].data_ptr()),
+             v(d["C"].data_ptr()), None, v(d["dy"].data_ptr()), None, *(v(t.data_ptr()) for t in out),
+             v(ws.data_ptr()), ws.numel(), b, L, D, N, _ffi.DTYPE[cfg["dtype"]], _ffi.DISC[cfg["disc"]],
+             v(stream.cuda_stream))
+    ms = []
+    for i in range(3 + reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        _ffi.check("ssm_scan_bwd", fn(*cargs))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            ms.append(e0.elapsed_time(e1))
+    lib.check_device()
+    med = statistics.median(ms) / 1e3
+    nbytes = bwd_bytes(cfg)
+    gbs = nbytes / med / 1e9
+    return {"workload": describe(name, cfg).split(";")[0] + "; backward (all input gradients)",
+            "launch_ms_median": med * 1e3, "elems_per_s": b * L * D / med, "gbs": gbs, "hbm_frac": gbs / peak,
+            "bytes_per_launch": nbytes, "workspace_bytes": need, "reps": reps}
 
 
 def measure_decode(steps, flush, peak):
@@ -568,6 +623,7 @@ def main(argv=None):
             if name != args.workload:
                 extra[name] = measure_prefill(name, 10, flush, peak)
         extra[args.workload + "_fused"] = measure_prefill(args.workload, 10, flush, peak, fused=True)
+        extra[args.workload + "_bwd"] = measure_backward(args.workload, 10, flush, peak)
         extra["decode"] = measure_decode(1000, flush, peak)
         line["workloads"] = extra
     if not args.no_cpu_baseline:

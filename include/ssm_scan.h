@@ -29,7 +29,9 @@
  *  - N (state size) must be in [1, 16]; larger N returns SSM_ERR_UNSUPPORTED.
  *  - Outputs may not overlap inputs (checked on the pointer ranges: SSM_ERR_INVALID_ARG).
  *  - Any status other than SSM_OK leaves a one-line reason in ssm_last_error() (per thread).
- *  - Results are deterministic for a given shape, dtype and device (no atomics on the data path).
+ *  - Results are deterministic for a given shape, dtype and device (no atomics on the data path), except
+ *    the sums over channels, batch and time of ssm_scan_bwd (dA_log, dB, dC), which use atomic adds whose
+ *    order may change the last bits from run to run.
  */
 #ifndef SSM_SCAN_H
 #define SSM_SCAN_H
@@ -113,6 +115,40 @@ ssm_status ssm_scan_step_ex(float *state, const void *x_t, const void *delta_t, 
                             const float *delta_bias, int delta_softplus, const float *D_skip, const void *z_t,
                             void *y_t, int64_t batch, int64_t D, int64_t N,
                             ssm_dtype dtype, ssm_disc disc, void *stream);
+
+/*
+ * Backward pass of the prefill scan: the gradients of
+ *     J = sum_{b,t,d} dy[b,t,d] y[b,t,d] + sum_{b,d,n} dfinal[b,d,n] final_state[b,d,n]
+ * with respect to every input of ssm_scan_fwd (plain scan: no softplus, feedthrough or gate). The states
+ * are recomputed from the inputs rather than read from a saved copy ("State Space Models & Mamba"
+ * chapter, the paragraph on the fused kernel: the backward pass recomputes h). The formulas are the
+ * chain rule of the forward recurrence run backwards in time through lambda_t = dJ/dh_t.
+ *   x, delta, A_log, B, C, h0   as in ssm_scan_fwd (h0 may be NULL: zero initial state)
+ *   dy          [batch, L, D]  dtype   gradient of J with respect to y
+ *   dfinal      [batch, D, N]  fp32    gradient with respect to final_state, or NULL (zero)
+ *   dx, ddelta  [batch, L, D]  dtype   outputs (bf16 rounded to nearest even)
+ *   dA_log      [D, N]         fp32    output (sums over the batch and the time axis)
+ *   dB, dC      [batch, L, N]  fp32    outputs (sums over the D channels)
+ *   dh0         [batch, D, N]  fp32    output, or NULL (not wanted); dfinal when L == 0
+ *   workspace   device memory of at least ssm_scan_bwd_workspace_size(batch, L, D, N) bytes (may be NULL
+ *               when that is 0), owned by the caller; its contents on entry do not matter and on return
+ *               are unspecified. It holds the states at chunk ends between the kernel's forward
+ *               recomputation and its backward walk. Two calls in flight may not share it.
+ * Outputs are overwritten (dA_log, dB and dC are zeroed on the stream first, then accumulated with atomic
+ * adds). No output may overlap an input, the workspace or another output. Other conventions and errors
+ * as for ssm_scan_fwd; a workspace that is NULL or too small returns SSM_ERR_INVALID_ARG.
+ */
+ssm_status ssm_scan_bwd(const void *x, const void *delta, const float *A_log,
+                        const void *B, const void *C, const float *h0,
+                        const void *dy, const float *dfinal,
+                        void *dx, void *ddelta, float *dA_log, float *dB, float *dC, float *dh0,
+                        void *workspace, size_t workspace_bytes,
+                        int64_t batch, int64_t L, int64_t D, int64_t N,
+                        ssm_dtype dtype, ssm_disc disc, void *stream);
+
+/* Bytes of workspace ssm_scan_bwd needs for these sizes (0 for sequences of at most 8 steps); 0 as well
+   for invalid sizes, which ssm_scan_bwd itself rejects. */
+size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t N);
 
 /* Synchronise `stream` and report any error raised while this library's kernels ran on it. */
 ssm_status ssm_check_device(void *stream);

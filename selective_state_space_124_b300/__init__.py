@@ -2,6 +2,7 @@
 
     y, final_state = ssm_scan_fwd(x, delta, A_log, B, C, disc="euler" | "zoh", h0=None)
     y_t = ssm_scan_step(state, x_t, delta_t, A_log, B_t, C_t, disc=...)   # state updated in place
+    grads = ssm_scan_bwd(x, delta, A_log, B, C, dy, disc=..., h0=None, dfinal=None)  # dict of gradients
 
 Both take the layer pieces the library can fuse around the scan, each optional: ``delta_bias`` [D] and
 ``delta_softplus`` (the scan uses softplus(delta + bias)), ``D_skip`` [D] (adds D x to y) and ``z`` (gates
@@ -18,8 +19,8 @@ from __future__ import annotations
 from . import _ffi
 from ._ffi import SsmError
 
-__all__ = ["ssm_scan_fwd", "ssm_scan_step", "ssm_scan_fwd_ptr", "ssm_scan_step_ptr", "check_device",
-           "SsmError", "version"]
+__all__ = ["ssm_scan_fwd", "ssm_scan_step", "ssm_scan_bwd", "ssm_scan_fwd_ptr", "ssm_scan_step_ptr",
+           "bwd_workspace_size", "check_device", "SsmError", "version"]
 
 
 def _torch():
@@ -152,6 +153,56 @@ def ssm_scan_step(state, x_t, delta_t, A_log, B_t, C_t, disc: str = "euler", *, 
                                       _ptr(y_t), batch, D, N, code, _ffi.DISC[disc], ctypes_void(s.cuda_stream))
     _ffi.check("ssm_scan_step", st)
     return y_t
+
+
+def bwd_workspace_size(batch: int, L: int, D: int, N: int) -> int:
+    """Bytes of device workspace ssm_scan_bwd needs for these sizes."""
+    return int(_ffi.load().ssm_scan_bwd_workspace_size(batch, L, D, N))
+
+
+def ssm_scan_bwd(x, delta, A_log, B, C, dy, disc: str = "euler", h0=None, dfinal=None, *, want_dh0: bool = True,
+                 workspace=None, stream=None):
+    """Gradients of sum(dy * y) + sum(dfinal * final_state) for the prefill scan (CUDA tensors).
+
+    Returns a dict: dx, ddelta [batch, L, D] in x's dtype; dA_log [D, N], dB, dC [batch, L, N] and dh0
+    [batch, D, N] (None unless ``want_dh0``) in float32. ``workspace`` (a uint8 CUDA tensor of at least
+    ``bwd_workspace_size(...)`` bytes) is allocated here when not given.
+    """
+    torch = _torch()
+    batch, L, D = x.shape
+    N = A_log.shape[-1]
+    code = _dtype_code(x)
+    for name, t in (("delta", delta), ("B", B), ("C", C), ("dy", dy)):
+        if t.dtype != x.dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, x has {x.dtype}")
+    for name, t in (("A_log", A_log), ("h0", h0), ("dfinal", dfinal)):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError(f"{name} must be float32")
+    if tuple(delta.shape) != (batch, L, D) or tuple(dy.shape) != (batch, L, D) or tuple(B.shape) != (batch, L, N) \
+            or tuple(C.shape) != (batch, L, N) or tuple(A_log.shape) != (D, N) \
+            or any(t is not None and tuple(t.shape) != (batch, D, N) for t in (h0, dfinal)):
+        raise ValueError("shape mismatch: x/delta/dy [b,L,D], B/C [b,L,N], A_log [D,N], h0/dfinal [b,D,N]")
+    ts = [t for t in (x, delta, A_log, B, C, dy, h0, dfinal) if t is not None]
+    if any(not t.is_contiguous() for t in ts) or any(t.device != x.device for t in ts) or x.device.type != "cuda":
+        raise ValueError("inputs must be contiguous CUDA tensors on one device")
+    dev = x.device
+    out = {"dx": torch.empty((batch, L, D), dtype=x.dtype, device=dev),
+           "ddelta": torch.empty((batch, L, D), dtype=x.dtype, device=dev),
+           "dA_log": torch.empty((D, N), dtype=torch.float32, device=dev),
+           "dB": torch.empty((batch, L, N), dtype=torch.float32, device=dev),
+           "dC": torch.empty((batch, L, N), dtype=torch.float32, device=dev),
+           "dh0": torch.empty((batch, D, N), dtype=torch.float32, device=dev) if want_dh0 else None}
+    need = bwd_workspace_size(batch, L, D, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = _ffi.load().ssm_scan_bwd(_ptr(x), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(h0), _ptr(dy),
+                                  _ptr(dfinal), _ptr(out["dx"]), _ptr(out["ddelta"]), _ptr(out["dA_log"]),
+                                  _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dh0"]), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), batch, L, D, N, code,
+                                  _ffi.DISC[disc], ctypes_void(s.cuda_stream))
+    _ffi.check("ssm_scan_bwd", st)
+    return out
 
 
 def check_device(stream=None) -> None:

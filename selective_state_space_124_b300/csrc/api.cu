@@ -149,6 +149,57 @@ ssm_status ssm_scan_step_ex(float* state, const void* x_t, const void* delta_t, 
   return SSM_OK;
 }
 
+size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t N) {
+  int64_t bl = 0, bld = 0, bldn = 0;
+  if (N < 1 || N > 16 || !mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bld, N, &bldn)) return 0;
+  if (bldn > INT64_MAX / 4) return 0;
+  return bwd_workspace_bytes(batch, L, D, N);
+}
+
+ssm_status ssm_scan_bwd(const void* x, const void* delta, const float* A_log, const void* B, const void* C,
+                        const float* h0, const void* dy, const float* dfinal, void* dx, void* ddelta, float* dA_log,
+                        float* dB, float* dC, float* dh0, void* workspace, size_t workspace_bytes, int64_t batch,
+                        int64_t L, int64_t D, int64_t N, ssm_dtype dtype, ssm_disc disc, void* stream) {
+  g_last_error[0] = '\0';
+  if (!valid_enums(dtype, disc)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_bwd: bad dtype or disc");
+  if (batch < 0 || L < 0 || D < 0 || N < 1)
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_bwd: bad sizes (batch %lld, L %lld, D %lld, N %lld)",
+                static_cast<long long>(batch), static_cast<long long>(L), static_cast<long long>(D),
+                static_cast<long long>(N));
+  if (N > 16) return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_bwd: N = %lld > 16", static_cast<long long>(N));
+  int64_t bl = 0, bld = 0, bln = 0, bdn = 0, dn = 0, bldn = 0;
+  if (!mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bl, N, &bln) || !mul_ok(batch * D, N, &bdn) ||
+      !mul_ok(D, N, &dn) || !mul_ok(bld, N, &bldn) || bldn > INT64_MAX / 4)
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_bwd: size overflow");
+  const int64_t es = dtype == SSM_DTYPE_BF16 ? 2 : 4;
+  if (bld > 0 && (!x || !delta || !dy || !dx || !ddelta))
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_bwd: null x, delta, dy, dx or ddelta");
+  if (bln > 0 && (!B || !C || !dB || !dC)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_bwd: null B, C, dB or dC");
+  if (dn > 0 && (!A_log || !dA_log)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_bwd: null A_log or dA_log");
+  const size_t need = bwd_workspace_bytes(batch, L, D, N);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_bwd: workspace of %zu bytes needed, %zu given", need,
+                workspace ? workspace_bytes : static_cast<size_t>(0));
+  const Range outs[] = {range_of(dx, bld, es), range_of(ddelta, bld, es), range_of(dA_log, dn, 4),
+                        range_of(dB, bln, 4), range_of(dC, bln, 4), range_of(dh0, dh0 ? bdn : 0, 4),
+                        range_of(workspace, static_cast<int64_t>(need), 1)};
+  const Range ins[] = {range_of(x, bld, es), range_of(delta, bld, es), range_of(A_log, dn, 4), range_of(B, bln, es),
+                       range_of(C, bln, es), range_of(h0, h0 ? bdn : 0, 4), range_of(dy, bld, es),
+                       range_of(dfinal, dfinal ? bdn : 0, 4)};
+  for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+    for (const Range& r : ins)
+      if (overlap(outs[i], r)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_bwd: outputs overlap inputs");
+    for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+      if (overlap(outs[i], outs[j])) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_bwd: outputs overlap each other");
+  }
+  BwdArgs a{x, delta, A_log, B, C, h0, dy, dfinal, dx, ddelta, dA_log, dB, dC, dh0,
+            static_cast<float*>(workspace), batch, L, D, N, static_cast<int>(dtype), static_cast<int>(disc),
+            static_cast<cudaStream_t>(stream)};
+  cudaError_t e = launch_bwd(a);
+  if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_bwd launch");
+  return SSM_OK;
+}
+
 ssm_status ssm_check_device(void* stream) {
   g_last_error[0] = '\0';
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

@@ -43,6 +43,28 @@ struct StepArgs {
   const void* z = nullptr;            // [batch, D] (dtype)
 };
 
+struct BwdArgs {
+  const void* x;
+  const void* delta;
+  const float* A_log;
+  const void* B;
+  const void* C;
+  const float* h0;      // or null
+  const void* dy;
+  const float* dfinal;  // or null
+  void* dx;
+  void* ddelta;
+  float* dA_log;
+  float* dB;
+  float* dC;
+  float* dh0;           // or null
+  float* workspace;     // bwd_workspace_bytes() bytes
+  int64_t batch, L, D, N;
+  int dtype;
+  int disc;
+  cudaStream_t stream;
+};
+
 int sm_count();  // multiprocessors of the current device (cached per device)
 
 cudaError_t launch_fwd_simple(const FwdArgs& a);
@@ -51,5 +73,7 @@ cudaError_t launch_fwd_tma(const FwdArgs& a);
 int read_and_clear_device_status();       // nonzero if a kernel recorded a failed bounded wait
 cudaError_t launch_init_state(const FwdArgs& a);  // final_state = h0 or 0 (used when L == 0)
 cudaError_t launch_step(const StepArgs& a);
+size_t bwd_workspace_bytes(int64_t batch, int64_t L, int64_t D, int64_t N);
+cudaError_t launch_bwd(const BwdArgs& a);
 
 }  // namespace ssm

@@ -1,0 +1,469 @@
+// scan_bwd.cu -- backward pass of the prefill scan: gradients of
+//     J = sum dy * y + sum dfinal * final_state
+// with respect to x, delta, A_log, B, C and h0, with the states recomputed rather than stored ("State Space
+// Models & Mamba" chapter, the paragraph on the fused kernel: the backward pass recomputes h_t instead of
+// keeping it). The gradient formulas are the chain rule of the forward recurrence h_t = Abar_t h_{t-1} +
+// Bbar_t x_t, y_t = C_t . h_t, run backwards through the adjoint lambda_t = dJ/dh_t:
+//     lambda_t = C_t dy_t + Abar_{t+1} lambda_{t+1}                 (lambda_{L-1} adds dfinal)
+//     dx_t = sum_n lambda Bbar,   dC_t,n = dy_t h_t,   dB_t,n = lambda x (Bbar / B)
+//     ddelta_t = sum_n lambda h_{t-1} A Abar + lambda x dBbar/ddelta,   dA_n = sum_t lambda h_{t-1} delta Abar
+//                + lambda x dBbar/dA,   dA_log = dA * A,   dh0 = Abar_0 lambda_0
+// with dBbar/ddelta = B (Euler) or Abar B (ZOH) and, for ZOH, dBbar/dA = B delta^2 f(delta A),
+// f(w) = (w e^w - (e^w - 1)) / w^2 (limit 1/2 at A = 0, the same continuous extension as Bbar there).
+//
+// Work layout: the forward kernels' split. One lane per channel, one warp per 32 consecutive channels of
+// one batch element (a row); the rows' time axes are laid end to end and cut into equal contiguous
+// pieces, one per warp. A piece [t0, t1) of a row:
+//   1. rebuilds h(t0-1) by the backward warm-up walk of the forward kernels (exact at t = 0);
+//   2. runs forward over [t0, t1), saving h at the end of every aligned chunk of kChunk steps that is
+//      followed by another chunk of the piece into the workspace (global memory; the only scratch);
+//   3. rebuilds mu = Abar_{t1} lambda_{t1} (the adjoint flowing into h_{t1-1} from later steps) by walking
+//      forward from t1: mu = sum_{j >= t1} (prod_{k=t1..j} Abar_k) (C_j dy_j + [j = L-1] dfinal), stopping
+//      once every decay product is below kCarryEps or at j = L - 1, where it is exact;
+//   4. walks the chunks backwards: recomputes the chunk's states from its saved start into shared memory
+//      (each lane its own column, so no lane reads another's and no barrier is needed), then steps back
+//      through the chunk accumulating the gradients.
+// dB and dC sum over channels: each warp reduces its 32 lanes' terms with a shuffle reduce-scatter and adds
+// the result into the outputs with one atomic add per (step, entry) per warp; dA_log sums over the batch
+// and the time axis: one atomic add per entry per piece. The three are zeroed by the entry point first.
+#include "common.cuh"
+#include "launch.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kBwdWarps = 8;       // warps per CTA
+constexpr int kChunk = 8;          // steps per recomputed chunk (shared-memory rows per warp: kChunk + 2)
+constexpr int kMinBwdPiece = 128;  // shortest piece worth a separate warp (each piece runs two warm-ups)
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct BwdParams {
+  const void* x;
+  const void* delta;
+  const float* A_log;
+  const void* B;
+  const void* C;
+  const float* h0;
+  const void* dy;
+  const float* dfinal;
+  void* dx;
+  void* ddelta;
+  float* dA_log;
+  float* dB;
+  float* dC;
+  float* dh0;
+  float* ws;        // [batch, nck, N, D] chunk-end states
+  int64_t batch, L, D, N;
+  int64_t nck;      // chunks per row that are followed by another: ceil(L / kChunk) - 1
+  int64_t groups;   // ceil(D / 32)
+  int64_t total;    // batch * groups * L
+  int64_t nwarps;
+};
+
+// f(w) = (w e^w - (e^w - 1)) / w^2 = sum_{m >= 2} (m - 1) w^(m-2) / m!: the Taylor series up to w^6 where the
+// difference would cancel (|w| < 1/4; the next term is below 2e-9 there), the difference itself elsewhere
+// (a = e^w, e = e^w - 1 computed without cancellation).
+__device__ __forceinline__ float zoh_dA_factor(float w, float a, float e) {
+  if (fabsf(w) < 0.25f) {
+    float q = fmaf(w, 1.0f / 5760.0f, 1.0f / 840.0f);
+    q = fmaf(w, q, 1.0f / 144.0f);
+    q = fmaf(w, q, 1.0f / 30.0f);
+    q = fmaf(w, q, 1.0f / 8.0f);
+    q = fmaf(w, q, 1.0f / 3.0f);
+    return fmaf(w, q, 0.5f);
+  }
+  return (w * a - e) / (w * w);
+}
+
+// floats of shared memory per warp: kChunk + 2 rows of NP x 32 states, then a chunk's x, delta and dy columns
+// and its B and C rows
+template <int NP>
+constexpr int kBwdWarpFloats = (kChunk + 2) * NP * 32 + 3 * kChunk * 32 + 2 * kChunk * 16;
+
+template <int NP, bool ZOH>
+struct BwdChan {
+  float A2[NP];    // A * log2(e)
+  float invA[NP];  // 1 / A (ZOH), 0 where A == 0
+};
+
+// Abar - 1 and Bbar / B of one entry at one step.
+template <int NP, bool ZOH>
+__device__ __forceinline__ void coefs(const BwdChan<NP, ZOH>& c, int n, float dt, float& a, float& e, float& bf) {
+  const float w = dt * c.A2[n];
+  a = ex2(w);
+  e = exp2m1(w, a);
+  if (ZOH) bf = c.A2[n] == 0.0f ? dt : e * c.invA[n];
+  else bf = dt;
+}
+
+// Sum over the warp of 32 values per lane (v[j], j < 32); lane l returns the total of v[l]. Recursive
+// halving: at each level a lane keeps the half of its values selected by one bit of its index and adds
+// the partner's copy of that half (16 + 8 + 4 + 2 + 1 shuffles).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
+#pragma unroll
+    for (int j = 0; j < w; ++j) {
+      const float send = up ? v[j] : v[j + w];
+      const float keep = up ? v[j + w] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
+// One chunk of at most kChunk consecutive steps [s, s + n) of a row, staged in this warp's shared memory for
+// the arithmetic: each lane's x, delta and dy in its own column (xs, ds, gs: [kChunk][32]), the shared B and C
+// rows in bs, cs ([kChunk][16]). All loads of a chunk are issued before any is stored, so a chunk costs one
+// memory round trip rather than one per step, and the step loops can stay rolled (small code) while still
+// indexing the chunk's steps.
+template <typename T, bool WX, bool WG, bool WB, bool WC>
+__device__ __forceinline__ void load_chunk(const BwdParams& p, int64_t b, int64_t d, bool act, int lane, int64_t s,
+                                           int n, float* xs, float* ds, float* gs, float* bs, float* cs) {
+  const int64_t base = (b * p.L + s) * p.D + d;
+  const int N = static_cast<int>(p.N);
+  const int64_t bc = (b * p.L + s) * p.N;
+  float xv[kChunk], dv[kChunk], gv[kChunk], bv[kChunk * 16 / 32], cv[kChunk * 16 / 32];
+#pragma unroll
+  for (int i = 0; i < kChunk; ++i) {
+    const bool ok = act && i < n;
+    if (WX) xv[i] = ok ? Elem<T>::load(p.x, base + static_cast<int64_t>(i) * p.D) : 0.0f;
+    dv[i] = ok ? Elem<T>::load(p.delta, base + static_cast<int64_t>(i) * p.D) : 0.0f;
+    if (WG) gv[i] = ok ? Elem<T>::load(p.dy, base + static_cast<int64_t>(i) * p.D) : 0.0f;
+  }
+#pragma unroll
+  for (int m = 0; m < kChunk * 16 / 32; ++m) {
+    const int k = lane + 32 * m, i = k >> 4, nn = k & 15;
+    const bool ok = i < n && nn < N;
+    if (WB) bv[m] = ok ? Elem<T>::load(p.B, bc + static_cast<int64_t>(i) * N + nn) : 0.0f;
+    if (WC) cv[m] = ok ? Elem<T>::load(p.C, bc + static_cast<int64_t>(i) * N + nn) : 0.0f;
+  }
+  __syncwarp();  // every lane has finished reading the previous chunk
+#pragma unroll
+  for (int i = 0; i < kChunk; ++i) {
+    if (WX) xs[i * 32 + lane] = xv[i];
+    ds[i * 32 + lane] = dv[i];
+    if (WG) gs[i * 32 + lane] = gv[i];
+  }
+#pragma unroll
+  for (int m = 0; m < kChunk * 16 / 32; ++m) {
+    if (WB) bs[lane + 32 * m] = bv[m];
+    if (WC) cs[lane + 32 * m] = cv[m];
+  }
+  __syncwarp();
+}
+
+template <int NP, bool ZOH, typename T>
+__global__ void __launch_bounds__(kBwdWarps * 32, 1) scan_bwd_kernel(BwdParams p) {
+  extern __shared__ float smem_bwd[];
+  const int lane = threadIdx.x & 31;
+  const int wid = threadIdx.x >> 5;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kBwdWarps + wid;
+  if (gw >= p.nwarps) return;  // whole warp leaves together
+  // this warp's shared memory: rows of states hs[(r * NP + n) * 32 + lane] (r = 0 the chunk's initial state,
+  // r = 1 + i after step i of the chunk, r = kChunk + 1 the piece's initial state), then the staged chunk
+  float* hs = smem_bwd + static_cast<size_t>(wid) * kBwdWarpFloats<NP>;
+  float* xs = hs + (kChunk + 2) * NP * 32;
+  float* ds = xs + kChunk * 32;
+  float* gs = ds + kChunk * 32;
+  float* bs = gs + kChunk * 32;
+  float* cs = bs + kChunk * 16;
+  auto hrow = [&](int r, int n) -> float& { return hs[(r * NP + n) * 32 + lane]; };
+  constexpr int kStart = kChunk + 1;
+
+  int64_t lo = static_cast<int64_t>(static_cast<__int128>(gw) * p.total / p.nwarps);
+  const int64_t hi = static_cast<int64_t>(static_cast<__int128>(gw + 1) * p.total / p.nwarps);
+  const int N = static_cast<int>(p.N);
+  const int64_t L = p.L, D = p.D;
+  while (lo < hi) {
+    const int64_t row = lo / L;
+    const int64_t t0 = lo % L;
+    const int64_t t1 = (hi - lo < L - t0) ? t0 + (hi - lo) : L;
+    lo += t1 - t0;
+    const int64_t b = row / p.groups;
+    const int64_t d = (row % p.groups) * 32 + lane;
+    const bool act = d < D;
+
+    BwdChan<NP, ZOH> c;
+#pragma unroll
+    for (int n = 0; n < NP; ++n) {
+      float A = -1.0f;
+      if (act && n < N) A = -ex2(__ldg(p.A_log + d * N + n) * kLog2e);
+      c.A2[n] = A * kLog2e;
+      c.invA[n] = A == 0.0f ? 0.0f : 1.0f / A;
+    }
+
+    // ---- 1. h(t0 - 1): walk back from t0 - 1 one chunk at a time ------------------------------------------
+    float h[NP];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) h[n] = 0.0f;
+    const float* h0row = p.h0 ? p.h0 + (b * D + d) * N : nullptr;
+    if (t0 > 0) {
+      float P[NP];
+#pragma unroll
+      for (int n = 0; n < NP; ++n) P[n] = 1.0f;
+      for (int64_t j = t0; j > 0;) {  // chunk [s, j)
+        const int64_t s = j > kChunk ? j - kChunk : 0;
+        const int cn = static_cast<int>(j - s);
+        load_chunk<T, true, false, true, false>(p, b, d, act, lane, s, cn, xs, ds, gs, bs, cs);
+#pragma unroll 1
+        for (int i = cn - 1; i >= 0; --i) {
+          const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
+#pragma unroll
+          for (int n = 0; n < NP; ++n) {
+            float a, e, bf;
+            coefs<NP, ZOH>(c, n, dt, a, e, bf);
+            h[n] = fmaf(P[n], bf * bs[i * 16 + n] * xv, h[n]);
+            P[n] = fmaf(P[n], e, P[n]);
+          }
+        }
+        j = s;
+        float pm = 0.0f;
+#pragma unroll
+        for (int n = 0; n < NP; ++n) pm = fmaxf(pm, fabsf(P[n]));
+        if (!act) pm = 0.0f;
+        if (j > 0 && !__any_sync(0xffffffffu, pm >= kCarryEps)) break;
+        if (j == 0 && h0row && act) {  // the walk reached t = 0: exact, plus the decayed initial state
+#pragma unroll
+          for (int n = 0; n < NP; ++n)
+            if (n < N) h[n] = fmaf(P[n], h0row[n], h[n]);
+        }
+      }
+    } else if (h0row && act) {
+#pragma unroll
+      for (int n = 0; n < NP; ++n)
+        if (n < N) h[n] = h0row[n];
+    }
+#pragma unroll
+    for (int n = 0; n < NP; ++n) hrow(kStart, n) = h[n];
+
+    // ---- 2. forward over the piece in aligned chunks, saving the state at each chunk end followed by another
+    for (int64_t ck = t0 / kChunk; ck * kChunk < t1; ++ck) {
+      const int64_t s = ck * kChunk > t0 ? ck * kChunk : t0;
+      const int64_t e_ = (ck + 1) * kChunk < t1 ? (ck + 1) * kChunk : t1;
+      const int cn = static_cast<int>(e_ - s);
+      load_chunk<T, true, false, true, false>(p, b, d, act, lane, s, cn, xs, ds, gs, bs, cs);
+#pragma unroll 1
+      for (int i = 0; i < cn; ++i) {
+        const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
+#pragma unroll
+        for (int n = 0; n < NP; ++n) {
+          float a, e, bf;
+          coefs<NP, ZOH>(c, n, dt, a, e, bf);
+          h[n] = fmaf(e, h[n], h[n]) + bf * bs[i * 16 + n] * xv;
+        }
+      }
+      if (e_ == (ck + 1) * kChunk && e_ < t1 && act) {  // chunk ck ends inside the piece
+        float* w = p.ws + ((b * p.nck + ck) * N) * D + d;
+#pragma unroll
+        for (int n = 0; n < NP; ++n)
+          if (n < N) w[static_cast<int64_t>(n) * D] = h[n];
+      }
+    }
+
+    // ---- 3. the adjoint entering from the right of the piece: walk forward from t1 one chunk at a time ----
+    float mu[NP];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) mu[n] = 0.0f;
+    const float* dfrow = p.dfinal ? p.dfinal + (b * D + d) * N : nullptr;
+    if (t1 == L) {
+      if (dfrow && act) {
+#pragma unroll
+        for (int n = 0; n < NP; ++n)
+          if (n < N) mu[n] = dfrow[n];
+      }
+    } else {
+      float P[NP];
+#pragma unroll
+      for (int n = 0; n < NP; ++n) P[n] = 1.0f;
+      for (int64_t j = t1; j < L;) {  // chunk [j, e_)
+        const int64_t e_ = j + kChunk < L ? j + kChunk : L;
+        const int cn = static_cast<int>(e_ - j);
+        load_chunk<T, false, true, false, true>(p, b, d, act, lane, j, cn, xs, ds, gs, bs, cs);
+#pragma unroll 1
+        for (int i = 0; i < cn; ++i) {
+          const float dt = ds[i * 32 + lane], g = gs[i * 32 + lane];
+#pragma unroll
+          for (int n = 0; n < NP; ++n) {
+            float a, e, bf;
+            coefs<NP, ZOH>(c, n, dt, a, e, bf);
+            P[n] = fmaf(P[n], e, P[n]);
+            mu[n] = fmaf(P[n], cs[i * 16 + n] * g, mu[n]);
+          }
+        }
+        j = e_;
+        if (j == L) {  // exact: add the final-state gradient, decayed through every step after t1 - 1
+          if (dfrow && act) {
+#pragma unroll
+            for (int n = 0; n < NP; ++n)
+              if (n < N) mu[n] = fmaf(P[n], dfrow[n], mu[n]);
+          }
+          break;
+        }
+        float pm = 0.0f;
+#pragma unroll
+        for (int n = 0; n < NP; ++n) pm = fmaxf(pm, fabsf(P[n]));
+        if (!act) pm = 0.0f;
+        if (!__any_sync(0xffffffffu, pm >= kCarryEps)) break;
+      }
+    }
+
+    // ---- 4. chunks backwards ----------------------------------------------------------------------------
+    float dA[NP];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) dA[n] = 0.0f;
+    for (int64_t ck = (t1 - 1) / kChunk; ck >= t0 / kChunk; --ck) {
+      const int64_t s = ck * kChunk > t0 ? ck * kChunk : t0;
+      const int64_t e_ = (ck + 1) * kChunk < t1 ? (ck + 1) * kChunk : t1;
+      const int cn = static_cast<int>(e_ - s);
+      load_chunk<T, true, true, true, true>(p, b, d, act, lane, s, cn, xs, ds, gs, bs, cs);
+      if (s == t0) {
+#pragma unroll
+        for (int n = 0; n < NP; ++n) h[n] = hrow(kStart, n);
+      } else {  // s = ck * kChunk > t0: chunk ck - 1 ends inside the piece; step 2 saved its state
+        const float* w = p.ws + ((b * p.nck + ck - 1) * N) * D + d;
+#pragma unroll
+        for (int n = 0; n < NP; ++n) h[n] = (act && n < N) ? w[static_cast<int64_t>(n) * D] : 0.0f;
+      }
+#pragma unroll
+      for (int n = 0; n < NP; ++n) hrow(0, n) = h[n];
+#pragma unroll 1
+      for (int i = 0; i < cn; ++i) {
+        const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
+#pragma unroll
+        for (int n = 0; n < NP; ++n) {
+          float a, e, bf;
+          coefs<NP, ZOH>(c, n, dt, a, e, bf);
+          h[n] = fmaf(e, h[n], h[n]) + bf * bs[i * 16 + n] * xv;
+          hrow(i + 1, n) = h[n];
+        }
+      }
+#pragma unroll 1
+      for (int i = cn - 1; i >= 0; --i) {
+        const int64_t t = s + i;
+        const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane], g = gs[i * 32 + lane];
+        float gx = 0.0f, gdt = 0.0f;
+        float v[32];  // this lane's terms of dB (v[n]) and dC (v[16 + n]) at step t
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          v[n] = 0.0f;
+          v[16 + n] = 0.0f;
+        }
+#pragma unroll
+        for (int n = 0; n < NP; ++n) {
+          const float bn = bs[i * 16 + n], cn_ = cs[i * 16 + n];
+          float a, e, bf;
+          coefs<NP, ZOH>(c, n, dt, a, e, bf);
+          const float An = c.A2[n] * kLn2;
+          const float lam = fmaf(cn_, g, mu[n]);
+          const float gb = lam * xv;           // dJ/dBbar
+          const float ga = lam * hrow(i, n);   // dJ/dAbar = lambda h_{t-1}
+          v[16 + n] = g * hrow(i + 1, n);      // dC term: dy h_t
+          v[n] = gb * bf;                      // dB term
+          gx = fmaf(lam * bf, bn, gx);
+          gdt = fmaf(ga * An, a, gdt);
+          dA[n] = fmaf(ga * dt, a, dA[n]);
+          if (ZOH) {
+            gdt = fmaf(gb * a, bn, gdt);
+            dA[n] = fmaf(gb * bn, dt * dt * zoh_dA_factor(dt * An, a, e), dA[n]);
+          } else {
+            gdt = fmaf(gb, bn, gdt);
+          }
+          mu[n] = a * lam;
+        }
+        if (act) {
+          const int64_t xi = (b * L + t) * D + d;
+          Elem<T>::store(p.dx, xi, gx);
+          Elem<T>::store(p.ddelta, xi, gdt);
+        }
+        const float tot = warp_reduce_scatter32(v, lane);  // lane l: total of v[l] over the warp
+        const int n_out = lane & 15;
+        if (n_out < N) atomicAdd((lane < 16 ? p.dB : p.dC) + (b * L + t) * N + n_out, tot);
+      }
+    }
+    if (act) {
+      if (t0 == 0 && p.dh0) {
+        float* out = p.dh0 + (b * D + d) * N;
+#pragma unroll
+        for (int n = 0; n < NP; ++n)
+          if (n < N) out[n] = mu[n];
+      }
+#pragma unroll
+      for (int n = 0; n < NP; ++n)
+        if (n < N) atomicAdd(p.dA_log + d * N + n, dA[n] * c.A2[n] * kLn2);
+    }
+  }
+}
+
+template <int NP, bool ZOH, typename T>
+cudaError_t launch_bwd_np(const BwdParams& bp, cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(kBwdWarps) * kBwdWarpFloats<NP> * sizeof(float);
+  auto kern = scan_bwd_kernel<NP, ZOH, T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = (bp.nwarps + kBwdWarps - 1) / kBwdWarps;
+  kern<<<static_cast<unsigned>(blocks), kBwdWarps * 32, smem, s>>>(bp);
+  return cudaGetLastError();
+}
+
+template <bool ZOH, typename T>
+cudaError_t launch_bwd_disc(const BwdParams& bp, cudaStream_t s) {
+  if (bp.N <= 4) return launch_bwd_np<4, ZOH, T>(bp, s);
+  if (bp.N <= 8) return launch_bwd_np<8, ZOH, T>(bp, s);
+  return launch_bwd_np<16, ZOH, T>(bp, s);
+}
+
+// dh0 = dfinal (or 0) when there are no steps.
+__global__ void copy_or_zero_kernel(const float* src, float* dst, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = src ? src[i] : 0.0f;
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int64_t batch, int64_t L, int64_t D, int64_t N) {
+  const int64_t nck = L > 0 ? (L + kChunk - 1) / kChunk - 1 : 0;
+  return static_cast<size_t>(batch) * static_cast<size_t>(nck) * static_cast<size_t>(N) * static_cast<size_t>(D) *
+         sizeof(float);
+}
+
+cudaError_t launch_bwd(const BwdArgs& a) {
+  cudaError_t e = cudaSuccess;
+  const size_t da_bytes = static_cast<size_t>(a.D * a.N) * sizeof(float);
+  if (da_bytes && (e = cudaMemsetAsync(a.dA_log, 0, da_bytes, a.stream)) != cudaSuccess) return e;
+  const size_t bc_bytes = static_cast<size_t>(a.batch * a.L * a.N) * sizeof(float);
+  if (bc_bytes) {
+    if ((e = cudaMemsetAsync(a.dB, 0, bc_bytes, a.stream)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(a.dC, 0, bc_bytes, a.stream)) != cudaSuccess) return e;
+  }
+  if (a.L == 0) {
+    const int64_t n = a.batch * a.D * a.N;
+    if (a.dh0 && n > 0) {
+      copy_or_zero_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, a.stream>>>(a.dfinal, a.dh0, n);
+      return cudaGetLastError();
+    }
+    return cudaSuccess;
+  }
+  BwdParams bp;
+  bp.x = a.x; bp.delta = a.delta; bp.A_log = a.A_log; bp.B = a.B; bp.C = a.C; bp.h0 = a.h0;
+  bp.dy = a.dy; bp.dfinal = a.dfinal;
+  bp.dx = a.dx; bp.ddelta = a.ddelta; bp.dA_log = a.dA_log; bp.dB = a.dB; bp.dC = a.dC; bp.dh0 = a.dh0;
+  bp.ws = a.workspace;
+  bp.batch = a.batch; bp.L = a.L; bp.D = a.D; bp.N = a.N;
+  bp.nck = (a.L + kChunk - 1) / kChunk - 1;
+  bp.groups = (a.D + 31) / 32;
+  const int64_t rows = a.batch * bp.groups;
+  bp.total = rows * a.L;
+  if (bp.total == 0) return cudaSuccess;  // no channels: the zeroed sums are the whole answer
+  int64_t nw = rows * ((a.L + kMinBwdPiece - 1) / kMinBwdPiece);
+  const int64_t want = static_cast<int64_t>(sm_count()) * kBwdWarps;
+  if (nw > want) nw = want;
+  if (nw < 1) nw = 1;
+  bp.nwarps = nw;
+  if (a.disc == 1)
+    return a.dtype == 1 ? launch_bwd_disc<true, __nv_bfloat16>(bp, a.stream) : launch_bwd_disc<true, float>(bp, a.stream);
+  return a.dtype == 1 ? launch_bwd_disc<false, __nv_bfloat16>(bp, a.stream) : launch_bwd_disc<false, float>(bp, a.stream);
+}
+
+}  // namespace ssm

@@ -81,6 +81,41 @@ def test_step_argument_errors(lib):
     assert lib.ssm_scan_step(*args, 0, 8, 16, 0, 0, None) == _ffi.SSM_OK
 
 
+def bwd(lib, *, ws=FAKE + (20 << 30), ws_bytes=1 << 30, dx=FAKE + (10 << 30), dB=FAKE + (13 << 30),
+        dy=FAKE + (8 << 30), batch=2, L=64, D=32, N=16, dtype=0, disc=1, dh0=FAKE + (15 << 30)):
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+    ins = [v(FAKE), v(FAKE + (1 << 30)), v(FAKE + (2 << 30)), v(FAKE + (3 << 30)), v(FAKE + (4 << 30)), None, v(dy),
+           None]
+    outs = [v(dx), v(FAKE + (11 << 30)), v(FAKE + (12 << 30)), v(dB), v(FAKE + (14 << 30)), v(dh0)]
+    return lib.ssm_scan_bwd(*ins, *outs, v(ws), ws_bytes, batch, L, D, N, dtype, disc, None)
+
+
+def test_bwd_workspace_size(lib):
+    # one saved state per (batch, chunk of 8 steps followed by another, entry, channel), fp32
+    assert lib.ssm_scan_bwd_workspace_size(2, 500, 128, 16) == 2 * (63 - 1) * 16 * 128 * 4
+    assert lib.ssm_scan_bwd_workspace_size(1, 8, 64, 16) == 0
+    assert lib.ssm_scan_bwd_workspace_size(1, 9, 64, 16) == 1 * 1 * 16 * 64 * 4
+    assert lib.ssm_scan_bwd_workspace_size(1, 0, 64, 16) == 0
+    assert lib.ssm_scan_bwd_workspace_size(1, 64, 64, 17) == 0  # unsupported N: the call itself rejects it
+
+
+def test_bwd_argument_errors(lib):
+    assert bwd(lib, N=17) == _ffi.SSM_ERR_UNSUPPORTED
+    assert bwd(lib, L=-1) == _ffi.SSM_ERR_INVALID_ARG
+    assert bwd(lib, dtype=5) == _ffi.SSM_ERR_INVALID_ARG
+    assert bwd(lib, dy=None) == _ffi.SSM_ERR_INVALID_ARG
+    assert bwd(lib, dB=None) == _ffi.SSM_ERR_INVALID_ARG
+    assert bwd(lib, ws=None) == _ffi.SSM_ERR_INVALID_ARG
+    assert b"workspace" in lib.ssm_last_error()
+    need = lib.ssm_scan_bwd_workspace_size(2, 64, 32, 16)
+    assert bwd(lib, ws_bytes=need - 1) == _ffi.SSM_ERR_INVALID_ARG
+    assert bwd(lib, dx=FAKE + 64) == _ffi.SSM_ERR_INVALID_ARG                 # dx overlaps x
+    assert bwd(lib, dh0=FAKE + (13 << 30) + 4) == _ffi.SSM_ERR_INVALID_ARG    # dh0 overlaps dB
+    assert b"each other" in lib.ssm_last_error()
+    assert bwd(lib, ws=FAKE + (10 << 30) + 8) == _ffi.SSM_ERR_INVALID_ARG      # workspace overlaps dx
+    assert bwd(lib, batch=1 << 40, L=1 << 20, D=1 << 20) == _ffi.SSM_ERR_INVALID_ARG
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         _ffi.load(str(tmp_path / "libssm_scan.so"))
