@@ -150,6 +150,30 @@ ssm_status ssm_scan_bwd(const void *x, const void *delta, const float *A_log,
    for invalid sizes, which ssm_scan_bwd itself rejects. */
 size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t N);
 
+/*
+ * ssm_scan_bwd without a workspace argument, for callers that cannot allocate device memory themselves:
+ * code running inside a host application whose memory pool owns the whole GPU and gives plugins no
+ * allocator, or a service that forbids allocation once it has started serving (a cudaMalloc there can
+ * stall or fail at the worst moment). It has no counterpart in the pages: it is a packaging choice of this
+ * library, not part of the method.
+ *
+ * The chunk-end states live in a scratch array inside the library itself (64 MiB, reserved on every
+ * device that loads the library until the process exits). Sizes whose ssm_scan_bwd_workspace_size()
+ * exceeds 64 MiB return SSM_ERR_INVALID_ARG with a message saying so (use ssm_scan_bwd with a workspace
+ * then). The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. The first
+ * call on a device looks up the array's device address on that device; make that first call before any
+ * stream capture. All calls on a device share the one array, so two calls whose kernels may run at the
+ * same time on that device (other streams, other host threads) race on it and give wrong gradients:
+ * serialise them. The array needs no clearing between calls (each call writes every entry it reads).
+ * Arguments, outputs and errors otherwise as for ssm_scan_bwd.
+ */
+ssm_status ssm_scan_bwd_noalloc(const void *x, const void *delta, const float *A_log,
+                                const void *B, const void *C, const float *h0,
+                                const void *dy, const float *dfinal,
+                                void *dx, void *ddelta, float *dA_log, float *dB, float *dC, float *dh0,
+                                int64_t batch, int64_t L, int64_t D, int64_t N,
+                                ssm_dtype dtype, ssm_disc disc, void *stream);
+
 /* Synchronise `stream` and report any error raised while this library's kernels ran on it. */
 ssm_status ssm_check_device(void *stream);
 

@@ -200,6 +200,26 @@ ssm_status ssm_scan_bwd(const void* x, const void* delta, const float* A_log, co
   return SSM_OK;
 }
 
+ssm_status ssm_scan_bwd_noalloc(const void* x, const void* delta, const float* A_log, const void* B, const void* C,
+                                const float* h0, const void* dy, const float* dfinal, void* dx, void* ddelta,
+                                float* dA_log, float* dB, float* dC, float* dh0, int64_t batch, int64_t L, int64_t D,
+                                int64_t N, ssm_dtype dtype, ssm_disc disc, void* stream) {
+  g_last_error[0] = '\0';
+  if (N >= 1 && N <= 16 && batch >= 0 && L >= 0 && D >= 0) {
+    const size_t need = ssm_scan_bwd_workspace_size(batch, L, D, N);
+    if (need > kBwdNoAllocScratchBytes)
+      return fail(SSM_ERR_INVALID_ARG,
+                  "ssm_scan_bwd_noalloc: these sizes need %zu bytes of scratch, the built-in scratch holds %zu "
+                  "(call ssm_scan_bwd with a workspace instead)",
+                  need, kBwdNoAllocScratchBytes);
+  }
+  void* scratch = nullptr;
+  const cudaError_t e = bwd_noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_bwd_noalloc: scratch address");
+  return ssm_scan_bwd(x, delta, A_log, B, C, h0, dy, dfinal, dx, ddelta, dA_log, dB, dC, dh0, scratch,
+                      kBwdNoAllocScratchBytes, batch, L, D, N, dtype, disc, stream);
+}
+
 ssm_status ssm_check_device(void* stream) {
   g_last_error[0] = '\0';
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

@@ -74,6 +74,8 @@ int read_and_clear_device_status();       // nonzero if a kernel recorded a fail
 cudaError_t launch_init_state(const FwdArgs& a);  // final_state = h0 or 0 (used when L == 0)
 cudaError_t launch_step(const StepArgs& a);
 size_t bwd_workspace_bytes(int64_t batch, int64_t L, int64_t D, int64_t N);
+constexpr size_t kBwdNoAllocScratchBytes = size_t(64) << 20;  // the built-in scratch of ssm_scan_bwd_noalloc
+cudaError_t bwd_noalloc_scratch(void** out);                     // its device address on the current device
 cudaError_t launch_bwd(const BwdArgs& a);
 
 }  // namespace ssm

@@ -26,6 +26,8 @@
 // dB and dC sum over channels: each warp reduces its 32 lanes' terms with a shuffle reduce-scatter and adds
 // the result into the outputs with one atomic add per (step, entry) per warp; dA_log sums over the batch
 // and the time axis: one atomic add per entry per piece. The three are zeroed by the entry point first.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -421,6 +423,35 @@ __global__ void copy_or_zero_kernel(const float* src, float* dst, int64_t n) {
 }
 
 }  // namespace
+
+// ---- built-in scratch for ssm_scan_bwd_noalloc ----------------------------------------------------------
+// A fixed array in the library's own device memory, for callers that cannot allocate a workspace. Every
+// device that loads the library holds it until the process exits; every call of ssm_scan_bwd_noalloc on a
+// device uses the same array.
+static __device__ __align__(256) unsigned char g_bwd_scratch[kBwdNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {nullptr};
+}  // namespace
+
+cudaError_t bwd_noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    // the array's name is only a host-side stand-in: its device address comes from the runtime, once per
+    // device, with that device current
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_bwd_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
 
 size_t bwd_workspace_bytes(int64_t batch, int64_t L, int64_t D, int64_t N) {
   const int64_t nck = L > 0 ? (L + kChunk - 1) / kChunk - 1 : 0;
