@@ -36,7 +36,7 @@ import ssm_inputs  # noqa: E402
 METRIC = "selective-scan B·L·D elems/s; achieved HBM GB/s as fraction of B300 peak"
 FALLBACK_HBM_GBS = 6400.0
 FLUSH_BYTES = 512 << 20
-FWD_SOURCES = ("scan_fwd_tma.cu", "common.cuh", "launch.h")  # the prefill kernel's own sources
+FWD_SOURCES = ("scan_fwd_tma.cu", "common.cuh")  # the prefill kernel's device code (host declarations excluded)
 
 
 def parse_args(argv=None):
