@@ -74,6 +74,8 @@ class Oracle:
         lib.oracle_scan_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32, vp, i64,
                                         vp, vp, vp, vp, vp, vp]
         lib.oracle_scan_bwd.restype = i32
+        lib.oracle_ssd_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp, vp]
+        lib.oracle_ssd_fwd.restype = i32
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         self.lib = lib
@@ -207,6 +209,29 @@ class Oracle:
                 "dh0": dh0.reshape(batch, D, N)}
 
 
+    def ssd_fwd(self, x, delta, A_log, B, C, disc="euler", h0=None, f64=None):
+        """Mamba-2 SSD layer (scalar A per head, see ssm_oracle.c): x [batch, L, H, P], delta [batch, L, H],
+        A_log [H], B, C [batch, L, N], h0 [batch, H, P, N] or None. Returns (y [batch, L, H, P],
+        final_state [batch, H, P, N]) in float64."""
+        arrs = [np.asarray(a) for a in (x, delta, A_log, B, C)]
+        if f64 is None:
+            f64 = any(a.dtype == np.float64 for a in arrs)
+        x, delta, A_log, B, C = (_as_input(a, f64) for a in arrs)
+        batch, L, H, P = x.shape
+        N = B.shape[-1]
+        assert delta.shape == (batch, L, H) and A_log.shape == (H,)
+        assert B.shape == (batch, L, N) and C.shape == (batch, L, N)
+        h0c = None if h0 is None else np.ascontiguousarray(np.asarray(h0, np.float64).reshape(batch, H, P, N))
+        y = np.empty((batch, L, H, P))
+        st = np.empty((batch, H, P, N))
+        rc = self.lib.oracle_ssd_fwd(x.ctypes.data, delta.ctypes.data, A_log.ctypes.data, B.ctypes.data,
+                                     C.ctypes.data, None if h0c is None else h0c.ctypes.data, batch, L, H, P, N,
+                                     DISC[disc], int(f64), y.ctypes.data, st.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle_ssd_fwd rejected its arguments")
+        return y, st
+
+
 _default: Oracle | None = None
 
 
@@ -227,6 +252,41 @@ def scan_step(*args, **kw):
 
 def scan_bwd(*args, **kw):
     return default().scan_bwd(*args, **kw)
+
+
+def ssd_fwd(*args, **kw):
+    return default().ssd_fwd(*args, **kw)
+
+
+def ssd_chunked(x, delta, A_log, B, C, Q, disc="euler", h0=None):
+    """The SSD layer evaluated the way the duality suggests ("Mathematical Prerequisites for Mamba" s7 and
+    the paragraph after it; "State Space Models & Mamba" chapter, the Mamba-2 paragraph): cut the sequence
+    into chunks of Q steps; inside a chunk, outputs are a masked matrix product with the 1-semiseparable
+    matrix L[i, j] = prod_{k=j+1..i} Abar_k = exp(s_i - s_j) (s the running sum of delta * A); between
+    chunks, the state is carried by the recurrence. numpy float64; shares no code with ssd_fwd.
+    Returns (y [batch, L, H, P], final_state [batch, H, P, N])."""
+    x, delta, A_log, B, C = (np.asarray(a, np.float64) for a in (x, delta, A_log, B, C))
+    batch, L, H, P = x.shape
+    N = B.shape[-1]
+    A = -np.exp(A_log)
+    y = np.zeros((batch, L, H, P))
+    fs = np.zeros((batch, H, P, N))
+    for b in range(batch):
+        for h in range(H):
+            S = np.zeros((N, P)) if h0 is None else np.asarray(h0, np.float64)[b, h].T.copy()  # [N, P]
+            for c0 in range(0, L, Q):
+                c1 = min(L, c0 + Q)
+                dt = delta[b, c0:c1, h]
+                w = dt * A[h]
+                s = np.cumsum(w)                                   # log of prod_{k <= i} Abar_k
+                _, coef = _discretise_np(dt, A[h], disc)
+                Xc = x[b, c0:c1, h, :] * coef[:, None]             # Bbar x, the B factor kept apart
+                Bc, Cc = B[b, c0:c1], C[b, c0:c1]
+                Lm = np.tril(np.exp(np.tril(s[:, None] - s[None, :])))  # exp(s_i - s_j), j <= i
+                y[b, c0:c1, h, :] = ((Cc @ Bc.T) * Lm) @ Xc + np.exp(s)[:, None] * (Cc @ S)
+                S = np.exp(s[-1]) * S + Bc.T @ (np.exp(s[-1] - s)[:, None] * Xc)
+            fs[b, h] = S.T
+    return y, fs
 
 
 def num_threads() -> int:

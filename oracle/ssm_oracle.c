@@ -323,3 +323,54 @@ int oracle_scan_bwd(const void *x, const void *delta, const void *A_log, const v
     }
     return bad ? -1 : 0;
 }
+
+/*
+ * ---- Mamba-2 structured state space duality (SSD) layer: the scan with A = a * I -----------------------
+ *
+ * "Mamba and Mamba-2" as the chapter describes it ("State Space Models & Mamba" chapter, the Mamba-2
+ * paragraph; "Mathematical Prerequisites for Mamba" s7 and the paragraph after it): the state matrix is a
+ * scalar times the identity, one scalar per head, so every channel of a head shares one decay per step and
+ * the head's state is a matrix [P, N] (P channels of the head, N state entries each):
+ *   A_h      = -exp(A_log[h])
+ *   abar     = exp(delta[b,t,h] * A_h)                      one decay per (step, head)
+ *   coef     = delta (Euler) or expm1(delta A_h) / A_h (ZOH; delta where A_h == 0)
+ *   S[p][n]  = abar * S[p][n] + coef * B[b,t,n] * x[b,t,h,p]
+ *   y[b,t,h,p] = sum_n C[b,t,n] * S[p][n]
+ * with S = h0 (or 0) before the first step and final_state = S after the last. This is the plain
+ * recurrence; the chunked (masked matrix product) evaluation of the same function lives in the tests.
+ * Layouts: x, y [batch, L, H, P]; delta [batch, L, H]; A_log [H]; B, C [batch, L, N] (one group shared by
+ * the heads); h0, final_state [batch, H, P, N] (doubles).
+ */
+int oracle_ssd_fwd(const void *x, const void *delta, const void *A_log, const void *B, const void *C,
+                   const double *h0, int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, int disc,
+                   int is_f64, double *y_out, double *state_out)
+{
+    if (batch < 0 || L < 0 || H < 0 || P < 1 || N < 1 || P > ORACLE_MAX_N || N > ORACLE_MAX_N) return -1;
+    if (disc != ORACLE_EULER && disc != ORACLE_ZOH) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t k = 0; k < batch * H; ++k) {
+        int64_t b = k / H, hh = k % H;
+        double *S = (double *)malloc((size_t)(P * N) * sizeof(double));
+        if (!S) { bad = 1; continue; }
+        double A = -exp(ld(A_log, hh, is_f64));
+        for (int64_t i = 0; i < P * N; ++i) S[i] = h0 ? h0[k * P * N + i] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            double dt = ld(delta, (b * L + t) * H + hh, is_f64);
+            double abar = exp(dt * A);
+            double coef = oracle_bfac(dt, A, disc);
+            for (int64_t p = 0; p < P; ++p) {
+                double xv = ld(x, ((b * L + t) * H + hh) * P + p, is_f64);
+                double yv = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    S[p * N + n] = abar * S[p * N + n] + coef * ld(B, (b * L + t) * N + n, is_f64) * xv;
+                    yv += ld(C, (b * L + t) * N + n, is_f64) * S[p * N + n];
+                }
+                y_out[((b * L + t) * H + hh) * P + p] = yv;
+            }
+        }
+        for (int64_t i = 0; i < P * N; ++i) state_out[k * P * N + i] = S[i];
+        free(S);
+    }
+    return bad ? -1 : 0;
+}

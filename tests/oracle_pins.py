@@ -499,10 +499,66 @@ def pin_bwd_split(orc):
         _close(g1["dh0"], g["dh0"], 1e-12, f"split dh0 ({disc})")
 
 
+# --- Mamba-2 SSD layer (scalar A per head) -----------------------------------------------------------------
+
+def _ssd_problem(rng, batch, L, H, P, N):
+    x = rng.standard_normal((batch, L, H, P))
+    dt = np.log1p(np.exp(rng.normal(-1.0, 1.0, (batch, L, H))))
+    A_log = rng.uniform(-1.0, 1.5, H)
+    B = rng.standard_normal((batch, L, N))
+    C = rng.standard_normal((batch, L, N))
+    h0 = rng.standard_normal((batch, H, P, N))
+    return x, dt, A_log, B, C, h0
+
+
+def pin_ssd_is_the_scan_with_shared_decay(orc):
+    """A = a I per head is the diagonal scan with A_log[d, n] = A_log[h] for all n and delta shared by the
+    head's P channels (d = h P + p): ssd_fwd equals scan_fwd on those broadcast arguments."""
+    rng = np.random.default_rng(41)
+    batch, L, H, P, N = 2, 19, 3, 4, 5
+    x, dt, A_log, B, C, h0 = _ssd_problem(rng, batch, L, H, P, N)
+    for disc in ("euler", "zoh"):
+        y, st = orc.ssd_fwd(x, dt, A_log, B, C, disc=disc, h0=h0, f64=True)
+        ym, sm = orc.scan_fwd(x.reshape(batch, L, H * P), np.repeat(dt, P, axis=2), np.repeat(A_log, P)[:, None]
+                              * np.ones((1, N)), B, C, disc=disc, h0=h0.reshape(batch, H * P, N), f64=True)
+        _close(y.reshape(batch, L, H * P), ym, 1e-13 * max(1.0, np.abs(ym).max()), f"ssd vs diagonal scan y ({disc})")
+        _close(st.reshape(batch, H * P, N), sm, 1e-13 * max(1.0, np.abs(sm).max()), f"ssd vs diagonal scan state ({disc})")
+
+
+def pin_ssd_chunked_duality(orc):
+    """The recurrence and the chunked masked-matrix evaluation are the same function for every chunk size
+    ("Mathematical Prerequisites for Mamba" s7: the recurrent and the matrix-multiply algorithms compute the
+    same output; SSD uses matrix products inside chunks and the recurrence between them)."""
+    rng = np.random.default_rng(42)
+    batch, L, H, P, N = 2, 23, 2, 3, 4
+    x, dt, A_log, B, C, h0 = _ssd_problem(rng, batch, L, H, P, N)
+    for disc in ("euler", "zoh"):
+        y, st = orc.ssd_fwd(x, dt, A_log, B, C, disc=disc, h0=h0, f64=True)
+        for Q in (1, 4, 8, 23, 64):
+            yc, sc = oracle_mod.ssd_chunked(x, dt, A_log, B, C, Q, disc=disc, h0=h0)
+            _close(yc, y, 1e-12 * max(1.0, np.abs(y).max()), f"chunked (Q = {Q}) vs recurrence y ({disc})")
+            _close(sc, st, 1e-12 * max(1.0, np.abs(st).max()), f"chunked (Q = {Q}) vs recurrence state ({disc})")
+
+
+def pin_ssd_running_example(orc):
+    """The pages' 1-SS numerical check: Abar = e^-1 (printed 0.368), Bbar = 1 - e^-1 (0.632), x = 1 gives
+    h = 0.632, 0.865, 0.950, 0.982 (closed form 1 - e^-t), here in every entry of a P x N head state."""
+    g = load("leaky_bucket.txt")
+    L, P, N = 12, 2, 3
+    y, st = orc.ssd_fwd(np.ones((1, L, 1, P)), np.ones((1, L, 1)), np.zeros(1), np.ones((1, L, N)),
+                        np.full((1, L, N), 1.0 / N), disc="zoh", f64=True)
+    exact = 1.0 - np.exp(-np.arange(1, L + 1, dtype=np.float64))
+    for p in range(P):
+        _close(y[0, :, 0, p], exact, 1e-13, "SSD running example vs 1 - e^-t")
+    _close(st[0, 0], np.full((P, N), exact[-1]), 1e-13, "SSD running example final state")
+    _close(y[0, :4, 0, 0], g["h"], 5e-4, "SSD running example vs printed samples")
+
+
 ALL_PINS = [
     pin_leaky_bucket_closed_form, pin_ema_identity, pin_euler_scalar_trace, pin_active_recall_traces,
     pin_lti_zoh_example, pin_convolution_view, pin_selective_zoh_example, pin_combine_tree,
     pin_small_delta_limit, pin_unit_input_two_step, pin_delta_limits, pin_brute_force_1ss,
     pin_split_and_step, pin_softplus_inside_scan, pin_feedthrough_and_gate, pin_bwd_finite_differences,
-    pin_bwd_convolution_adjoint, pin_bwd_one_step, pin_bwd_split,
+    pin_bwd_convolution_adjoint, pin_bwd_one_step, pin_bwd_split, pin_ssd_is_the_scan_with_shared_decay,
+    pin_ssd_chunked_duality, pin_ssd_running_example,
 ]

@@ -54,6 +54,15 @@ MUTANTS = {
                                    "dC_out[(k * L + t) * N + n] = dyt * hprev;"),
     "bwd_dx_missing_B": ("gx += lam[n] * bfac * Bn;", "gx += lam[n] * bfac;"),
     "bwd_dh0_undecayed": ("if (dh0_out) dh0_out[k * N + n] = mu[n];", "if (dh0_out) dh0_out[k * N + n] = lam[n];"),
+    "ssd_decay_dropped": ("S[p * N + n] = abar * S[p * N + n] + coef", "S[p * N + n] = S[p * N + n] + coef"),
+    "ssd_x_of_wrong_head": ("double xv = ld(x, ((b * L + t) * H + hh) * P + p, is_f64);",
+                            "double xv = ld(x, ((b * L + t) * H + (hh + 1) % H) * P + p, is_f64);"),
+    "ssd_delta_of_head_zero": ("double dt = ld(delta, (b * L + t) * H + hh, is_f64);",
+                               "double dt = ld(delta, (b * L + t) * H, is_f64);"),
+    "ssd_readout_uses_B": ("yv += ld(C, (b * L + t) * N + n, is_f64) * S[p * N + n];",
+                           "yv += ld(B, (b * L + t) * N + n, is_f64) * S[p * N + n];"),
+    "ssd_h0_ignored": ("for (int64_t i = 0; i < P * N; ++i) S[i] = h0 ? h0[k * P * N + i] : 0.0;",
+                       "for (int64_t i = 0; i < P * N; ++i) S[i] = 0.0;"),
     "channel_index_swapped": ("int64_t b = flat / D, d = flat % D;\n        double h[",
                               "int64_t d = flat / D, b = flat % D;\n        double h["),
 }
