@@ -53,7 +53,9 @@ def parse_args(argv=None):
     ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
                     help="override a size of the workload (batch, L or D), e.g. for a small profiling case")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the other prefill workloads and the decode workload (reported under 'workloads')")
+                    help="skip the other workloads (reported under 'workloads')")
+    ap.add_argument("--extra", default="all", metavar="KIND[,KIND]",
+                    help="which other workloads to time: all, or any of prefill, fused, bwd, ssd, decode")
     return ap.parse_args(argv)
 
 
@@ -69,6 +71,15 @@ def measured_peaks():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s (burst) from MEASURED_PEAKS.json, else None."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def fwd_bytes(cfg):
@@ -328,6 +339,65 @@ def measure_backward(name, reps, flush, peak):
     return {"workload": describe(name, cfg).split(";")[0] + "; backward (all input gradients)",
             "launch_ms_median": med * 1e3, "elems_per_s": b * L * D / med, "gbs": gbs, "hbm_frac": gbs / peak,
             "bytes_per_launch": nbytes, "workspace_bytes": need, "reps": reps}
+
+
+def ssd_bytes(cfg):
+    """Compulsory bytes of one SSD launch: x, B, C (bf16), delta (fp32), A_log read; y (bf16) and the final
+    state (fp32) written."""
+    b, L, H, P, N = cfg["batch"], cfg["L"], cfg["H"], cfg["P"], cfg["N"]
+    return 2 * b * L * H * P * 2 + 2 * b * L * N * 2 + b * L * H * 4 + H * 4 + b * H * P * N * 4
+
+
+def ssd_flops(cfg, Q=64):
+    """Tensor-core work of the chunked algorithm per launch, per chunk and head: C B^T (2 Q^2 N), the masked
+    product with x (2 Q^2 P), the inter-chunk read-out C S (2 Q N P) and the state update B^T x (2 Q N P),
+    full tiles (the causal halves are counted whole, as a dense evaluation would do them)."""
+    b, L, H, P, N = cfg["batch"], cfg["L"], cfg["H"], cfg["P"], cfg["N"]
+    chunks = (L + Q - 1) // Q
+    return b * H * chunks * (2 * Q * Q * N + 2 * Q * Q * P + 4 * Q * N * P)
+
+
+def measure_ssd(name, reps, flush, peak):
+    """The Mamba-2 SSD layer (ssm_ssd_fwd), timed like the prefill: L2 flushed before each launch, CUDA events.
+    Reports the HBM fraction of the compulsory bytes and the tensor throughput of the chunked algorithm."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    cfg = dict(ssm_inputs.SSD_WORKLOADS[name])
+    inp = ssm_inputs.make_ssd_inputs(**cfg)
+    b, L, H, P, N = cfg["batch"], cfg["L"], cfg["H"], cfg["P"], cfg["N"]
+
+    def bf(bits, shape):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).reshape(shape).cuda()
+    x, B, C = bf(inp["x_bits"], (b, L, H, P)), bf(inp["B_bits"], (b, L, N)), bf(inp["C_bits"], (b, L, N))
+    dt, A = torch.from_numpy(inp["delta"]).cuda(), torch.from_numpy(inp["A_log"]).cuda()
+    y = torch.empty((b, L, H, P), dtype=torch.bfloat16, device="cuda")
+    fs = torch.empty((b, H, P, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    args = [t.data_ptr() for t in (x, dt, A, B, C)] + [0, y.data_ptr(), fs.data_ptr()]
+    from selective_state_space_124_b300 import _ffi
+    fn = _ffi.load().ssm_ssd_fwd
+    import ctypes
+    cargs = [ctypes.c_void_p(a) if a else None for a in args] + [b, L, H, P, N, _ffi.DTYPE["bf16"],
+                                                                 _ffi.DISC[cfg["disc"]], ctypes.c_void_p(stream.cuda_stream)]
+    ms = []
+    for i in range(3 + reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        _ffi.check("ssm_ssd_fwd", fn(*cargs))
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            ms.append(e0.elapsed_time(e1))
+    lib.check_device()
+    med = statistics.median(ms) / 1e3
+    nbytes, flops = ssd_bytes(cfg), ssd_flops(cfg)
+    bf16_peak = measured_tensor_peak()
+    return {"workload": f"{name}: Mamba-2 SSD layer, batch {b}, L {L}, {H} heads x {P}, N {N}, bf16, {cfg['disc']}, "
+                        f"chunks of 64", "launch_ms_median": med * 1e3, "elems_per_s": b * L * H * P / med,
+            "gbs": nbytes / med / 1e9, "hbm_frac": nbytes / med / 1e9 / peak, "bytes_per_launch": nbytes,
+            "tflops": flops / med / 1e12, "tensor_frac": flops / med / 1e12 / bf16_peak if bf16_peak else None,
+            "flops_per_launch": flops, "reps": reps}
 
 
 def measure_decode(steps, flush, peak):
@@ -618,13 +688,20 @@ def main(argv=None):
         "gpu_launches": 2 * K,
     }
     if not args.no_extra and world == 1:
+        kinds = set(args.extra.split(",")) if args.extra != "all" else {"prefill", "fused", "bwd", "ssd", "decode"}
         extra = {}
-        for name in ("long", "mamba1p4b"):
-            if name != args.workload:
-                extra[name] = measure_prefill(name, 10, flush, peak)
-        extra[args.workload + "_fused"] = measure_prefill(args.workload, 10, flush, peak, fused=True)
-        extra[args.workload + "_bwd"] = measure_backward(args.workload, 10, flush, peak)
-        extra["decode"] = measure_decode(1000, flush, peak)
+        if "prefill" in kinds:
+            for name in ("long", "mamba1p4b"):
+                if name != args.workload:
+                    extra[name] = measure_prefill(name, 10, flush, peak)
+        if "fused" in kinds:
+            extra[args.workload + "_fused"] = measure_prefill(args.workload, 10, flush, peak, fused=True)
+        if "bwd" in kinds:
+            extra[args.workload + "_bwd"] = measure_backward(args.workload, 10, flush, peak)
+        if "ssd" in kinds:
+            extra["mamba2_130m_ssd"] = measure_ssd("mamba2_130m", 10, flush, peak)
+        if "decode" in kinds:
+            extra["decode"] = measure_decode(1000, flush, peak)
         line["workloads"] = extra
     if not args.no_cpu_baseline:
         r, cores, sample = cpu_oracle_rate(inp, cfg, oracle_sample(inp, cfg, args.cpu_seconds))

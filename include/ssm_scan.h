@@ -174,6 +174,29 @@ ssm_status ssm_scan_bwd_noalloc(const void *x, const void *delta, const float *A
                                 int64_t batch, int64_t L, int64_t D, int64_t N,
                                 ssm_dtype dtype, ssm_disc disc, void *stream);
 
+/*
+ * Mamba-2 SSD layer: the scan with A = a I, one scalar a per head, evaluated in chunks ("State Space Models
+ * & Mamba" chapter, the Mamba-2 paragraph; "Mathematical Prerequisites for Mamba" s7: the recurrence is a
+ * 1-semiseparable matrix product, computed as masked matrix products inside chunks of 64 steps on the
+ * tensor cores, with the recurrence carrying the state between chunks). For head h with state S [P, N]:
+ *   A_h = -exp(A_log[h]),  Abar = exp(delta[b,t,h] A_h),  coef = delta (Euler) or (Abar - 1) / A_h (ZOH)
+ *   S[p][n] = Abar S[p][n] + coef B[b,t,n] x[b,t,h,p],   y[b,t,h,p] = sum_n C[b,t,n] S[p][n]
+ *   x, y        [batch, L, H, P]  bf16 (dtype must be SSM_DTYPE_BF16)
+ *   delta       [batch, L, H]     fp32
+ *   A_log       [H]               fp32
+ *   B, C        [batch, L, N]     bf16, one group shared by every head
+ *   h0          [batch, H, P, N]  fp32 initial state, or NULL
+ *   final_state [batch, H, P, N]  fp32, or NULL
+ * N must be 64 or 128 and P a multiple of 16 (else SSM_ERR_UNSUPPORTED); x, B, C and y must be 16-byte
+ * aligned (else SSM_ERR_UNSUPPORTED). The products run with bf16 operands and fp32 accumulation (the
+ * masked score tile and a bf16 copy of the carried state are rounded to bf16 as operands; the state itself
+ * is carried in fp32). Other conventions as for ssm_scan_fwd.
+ */
+ssm_status ssm_ssd_fwd(const void *x, const float *delta, const float *A_log, const void *B, const void *C,
+                       const float *h0, void *y, float *final_state,
+                       int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N,
+                       ssm_dtype dtype, ssm_disc disc, void *stream);
+
 /* Synchronise `stream` and report any error raised while this library's kernels ran on it. */
 ssm_status ssm_check_device(void *stream);
 

@@ -3,6 +3,7 @@
     y, final_state = ssm_scan_fwd(x, delta, A_log, B, C, disc="euler" | "zoh", h0=None)
     y_t = ssm_scan_step(state, x_t, delta_t, A_log, B_t, C_t, disc=...)   # state updated in place
     grads = ssm_scan_bwd(x, delta, A_log, B, C, dy, disc=..., h0=None, dfinal=None)  # dict of gradients
+    y, final_state = ssm_ssd_fwd(x, delta, A_log, B, C, disc=..., h0=None)   # Mamba-2 SSD layer (bf16)
 
 Both take the layer pieces the library can fuse around the scan, each optional: ``delta_bias`` [D] and
 ``delta_softplus`` (the scan uses softplus(delta + bias)), ``D_skip`` [D] (adds D x to y) and ``z`` (gates
@@ -20,7 +21,7 @@ from . import _ffi
 from ._ffi import SsmError
 
 __all__ = ["ssm_scan_fwd", "ssm_scan_step", "ssm_scan_bwd", "ssm_scan_fwd_ptr", "ssm_scan_step_ptr",
-           "bwd_workspace_size", "check_device", "SsmError", "version"]
+           "bwd_workspace_size", "ssm_ssd_fwd", "check_device", "SsmError", "version"]
 
 
 def _torch():
@@ -203,6 +204,32 @@ def ssm_scan_bwd(x, delta, A_log, B, C, dy, disc: str = "euler", h0=None, dfinal
                                   _ffi.DISC[disc], ctypes_void(s.cuda_stream))
     _ffi.check("ssm_scan_bwd", st)
     return out
+
+
+def ssm_ssd_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, want_final_state: bool = True, stream=None):
+    """Mamba-2 SSD layer (scalar A per head), CUDA tensors: x [batch, L, H, P] bf16, delta [batch, L, H]
+    float32, A_log [H] float32, B, C [batch, L, N] bf16, h0 [batch, H, P, N] float32 or None. Returns
+    (y [batch, L, H, P] bf16, final_state [batch, H, P, N] float32 or None)."""
+    torch = _torch()
+    batch, L, H, P = x.shape
+    N = B.shape[-1]
+    if x.dtype != torch.bfloat16 or B.dtype != torch.bfloat16 or C.dtype != torch.bfloat16:
+        raise TypeError("x, B and C must be bfloat16")
+    if delta.dtype != torch.float32 or A_log.dtype != torch.float32 or (h0 is not None and h0.dtype != torch.float32):
+        raise TypeError("delta, A_log and h0 must be float32")
+    if tuple(delta.shape) != (batch, L, H) or tuple(A_log.shape) != (H,) or tuple(B.shape) != (batch, L, N) \
+            or tuple(C.shape) != (batch, L, N) or (h0 is not None and tuple(h0.shape) != (batch, H, P, N)):
+        raise ValueError("shape mismatch: x [b,L,H,P], delta [b,L,H], A_log [H], B/C [b,L,N], h0 [b,H,P,N]")
+    ts = [t for t in (x, delta, A_log, B, C, h0) if t is not None]
+    if any(not t.is_contiguous() for t in ts) or any(t.device != x.device for t in ts) or x.device.type != "cuda":
+        raise ValueError("inputs must be contiguous CUDA tensors on one device")
+    y = torch.empty((batch, L, H, P), dtype=torch.bfloat16, device=x.device)
+    fs = torch.empty((batch, H, P, N), dtype=torch.float32, device=x.device) if want_final_state else None
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    st = _ffi.load().ssm_ssd_fwd(_ptr(x), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(h0), _ptr(y), _ptr(fs),
+                                 batch, L, H, P, N, _ffi.DTYPE["bf16"], _ffi.DISC[disc], ctypes_void(s.cuda_stream))
+    _ffi.check("ssm_ssd_fwd", st)
+    return y, fs
 
 
 def check_device(stream=None) -> None:

@@ -220,6 +220,44 @@ ssm_status ssm_scan_bwd_noalloc(const void* x, const void* delta, const float* A
                       kBwdNoAllocScratchBytes, batch, L, D, N, dtype, disc, stream);
 }
 
+ssm_status ssm_ssd_fwd(const void* x, const float* delta, const float* A_log, const void* B, const void* C,
+                       const float* h0, void* y, float* final_state, int64_t batch, int64_t L, int64_t H, int64_t P,
+                       int64_t N, ssm_dtype dtype, ssm_disc disc, void* stream) {
+  g_last_error[0] = '\0';
+  if (!valid_enums(dtype, disc)) return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: bad dtype or disc");
+  if (batch < 0 || L < 0 || H < 0 || P < 1 || N < 1)
+    return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: bad sizes (batch %lld, L %lld, H %lld, P %lld, N %lld)",
+                static_cast<long long>(batch), static_cast<long long>(L), static_cast<long long>(H),
+                static_cast<long long>(P), static_cast<long long>(N));
+  if (dtype != SSM_DTYPE_BF16) return fail(SSM_ERR_UNSUPPORTED, "ssm_ssd_fwd: x, B, C and y must be bf16");
+  if (!ssd_shape_ok(P, N))
+    return fail(SSM_ERR_UNSUPPORTED, "ssm_ssd_fwd: needs N = 64 or 128 and P a multiple of 16 (N %lld, P %lld)",
+                static_cast<long long>(N), static_cast<long long>(P));
+  int64_t bl = 0, blh = 0, blhp = 0, bln = 0, bh = 0, bhpn = 0;
+  if (!mul_ok(batch, L, &bl) || !mul_ok(bl, H, &blh) || !mul_ok(blh, P, &blhp) || !mul_ok(bl, N, &bln) ||
+      !mul_ok(batch, H, &bh) || !mul_ok(bh * P, N, &bhpn) || bh * (P / 16) > INT32_MAX)
+    return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: size overflow");
+  if (blhp > 0 && (!x || !delta || !y)) return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: null x, delta or y");
+  if (bln > 0 && (!B || !C)) return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: null B or C");
+  if (H > 0 && !A_log) return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: null A_log");
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(B) |
+                        reinterpret_cast<uintptr_t>(C) | reinterpret_cast<uintptr_t>(y);
+  if (mis & 15) return fail(SSM_ERR_UNSUPPORTED, "ssm_ssd_fwd: x, B, C and y must be 16-byte aligned");
+  const Range ry = range_of(y, blhp, 2);
+  const Range rf = range_of(final_state, final_state ? bhpn : 0, 4);
+  const Range ins[] = {range_of(x, blhp, 2), range_of(delta, blh, 4), range_of(A_log, H, 4), range_of(B, bln, 2),
+                       range_of(C, bln, 2), range_of(h0, h0 ? bhpn : 0, 4)};
+  for (const Range& r : ins)
+    if (overlap(ry, r) || overlap(rf, r)) return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: outputs overlap inputs");
+  if (overlap(ry, rf)) return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: y overlaps final_state");
+  if (bh == 0) return SSM_OK;
+  SsdArgs a{x, delta, A_log, B, C, h0, y, final_state, batch, L, H, P, N, static_cast<int>(disc),
+            static_cast<cudaStream_t>(stream)};
+  cudaError_t e = launch_ssd(a);
+  if (e != cudaSuccess) return cuda_fail(e, "ssm_ssd_fwd launch");
+  return SSM_OK;
+}
+
 ssm_status ssm_check_device(void* stream) {
   g_last_error[0] = '\0';
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

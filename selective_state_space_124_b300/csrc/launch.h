@@ -65,6 +65,20 @@ struct BwdArgs {
   cudaStream_t stream;
 };
 
+struct SsdArgs {
+  const void* x;        // [batch, L, H, P] bf16
+  const float* delta;   // [batch, L, H]
+  const float* A_log;   // [H]
+  const void* B;        // [batch, L, N] bf16
+  const void* C;
+  const float* h0;      // [batch, H, P, N] or null
+  void* y;              // [batch, L, H, P] bf16
+  float* final_state;   // [batch, H, P, N] or null
+  int64_t batch, L, H, P, N;
+  int disc;
+  cudaStream_t stream;
+};
+
 int sm_count();  // multiprocessors of the current device (cached per device)
 
 cudaError_t launch_fwd_simple(const FwdArgs& a);
@@ -77,5 +91,7 @@ size_t bwd_workspace_bytes(int64_t batch, int64_t L, int64_t D, int64_t N);
 constexpr size_t kBwdNoAllocScratchBytes = size_t(64) << 20;  // the built-in scratch of ssm_scan_bwd_noalloc
 cudaError_t bwd_noalloc_scratch(void** out);                     // its device address on the current device
 cudaError_t launch_bwd(const BwdArgs& a);
+bool ssd_shape_ok(int64_t P, int64_t N);  // N in {64, 128}, P a multiple of 16
+cudaError_t launch_ssd(const SsdArgs& a);
 
 }  // namespace ssm

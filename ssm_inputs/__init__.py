@@ -12,6 +12,10 @@ Recipe (every workload, seed 0 unless stated; numpy PCG64 ``default_rng(seed)``;
   4. C      ~ N(0, 1)                          shape [batch, L, N]
   A_log[d, n] = log(n + 1) for every channel d (so A = -(n + 1)); not random.
   bf16 workloads: x, delta, B, C rounded float32 -> bf16 (round to nearest, ties to even).
+Mamba-2 SSD layer (``make_ssd_inputs``; scalar A per head): x ~ N(0, 1) [batch, L, H, P],
+  z ~ N(mu, sigma) -> delta = softplus(z) [batch, L, H] (float32), B ~ N(0, 1) [batch, L, N],
+  C ~ N(0, 1) [batch, L, N], then A_log[h] = log(u), u ~ U(1, 16) [H] (A between -16 and -1, the range
+  Mamba-2 initialises A in); x, B, C rounded to bf16 (the tensor-core operands), delta and A_log fp32.
 Decode workload: after A_log, the state [batch, D, N] ~ N(0, 1), then per step (in step order)
   x_t ~ N(0, 1) [batch, D], z_t ~ N(mu, sigma) -> delta_t = softplus(z_t) [batch, D],
   B_t ~ N(0, 1) [batch, N], C_t ~ N(0, 1) [batch, N].
@@ -34,6 +38,12 @@ WORKLOADS = {
     "long": dict(batch=1, L=131072, D=1536, N=16, dtype="f32", disc="zoh", mu=-4.0, sigma=1.0),
     # recurrent decode: batch 128, D 5120, N 16, fp32 state, 1000 steps
     "decode": dict(batch=128, L=1, D=5120, N=16, dtype="f32", disc="euler", mu=-2.0, sigma=1.0, steps=1000),
+}
+
+# Mamba-2 SSD layers: batch, L, heads H, head dimension P, state N (one B/C group), bf16 x/B/C/y.
+SSD_WORKLOADS = {
+    # Mamba-2-130M-shaped layer: d_inner 1536 = 24 heads x 64, N 128
+    "mamba2_130m": dict(batch=2, L=2048, H=24, P=64, N=128, disc="euler", mu=-2.0, sigma=1.0),
 }
 
 _CHUNK = 1 << 24
@@ -128,3 +138,17 @@ class DecodeStream:
         B = _normal(self.rng, (self.batch, self.N))
         C = _normal(self.rng, (self.batch, self.N))
         return dict(x=x, delta=delta, B=B, C=C)
+
+
+def make_ssd_inputs(batch, L, H, P, N, seed=0, mu=-2.0, sigma=1.0, **_):
+    """Draw an SSD layer's inputs per the recipe above. Returns float32 arrays x, delta, B, C, A_log (x, B,
+    C hold exactly bf16 values; their bit patterns under x_bits, B_bits, C_bits)."""
+    rng = np.random.default_rng(seed)
+    out = dict(x=_normal(rng, (batch, L, H, P)), delta=_softplus_f32(_normal(rng, (batch, L, H), mu, sigma)),
+               B=_normal(rng, (batch, L, N)), C=_normal(rng, (batch, L, N)))
+    out["A_log"] = np.log(rng.uniform(1.0, 16.0, H)).astype(np.float32)
+    for k in ("x", "B", "C"):
+        bits = bf16_round(out[k])
+        out[k + "_bits"] = bits
+        out[k] = bf16_to_f32(bits).reshape(out[k].shape)
+    return out

@@ -1,0 +1,75 @@
+"""Parity of the Mamba-2 SSD layer (ssm_ssd_fwd, chunked, tensor-core products) with the fp64 oracle's plain
+recurrence: both discretisations, with and without an initial state, sequences that end inside a chunk,
+shorter than one chunk and empty, N = 64 and 128, several channel blocks per head, and the full
+Mamba-2-130M-shaped layer."""
+import numpy as np
+import pytest
+
+import ssm_inputs
+from tolerance import TOL, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(torch, a_bits, shape):
+    return torch.from_numpy(a_bits.view(np.int16).copy()).view(torch.bfloat16).reshape(shape).cuda()
+
+
+def _run(orc, batch, L, H, P, N, disc, with_h0, seed):
+    import torch
+    import selective_state_space_124_b300 as lib
+    inp = ssm_inputs.make_ssd_inputs(batch, L, H, P, N, seed=seed)
+    h0 = np.random.default_rng(seed + 1).standard_normal((batch, H, P, N)).astype(np.float32) if with_h0 else None
+    x = _bf16(torch, inp["x_bits"], (batch, L, H, P))
+    B = _bf16(torch, inp["B_bits"], (batch, L, N))
+    C = _bf16(torch, inp["C_bits"], (batch, L, N))
+    dt = torch.from_numpy(inp["delta"]).cuda()
+    A = torch.from_numpy(inp["A_log"]).cuda()
+    y, fs = lib.ssm_ssd_fwd(x, dt, A, B, C, disc=disc, h0=None if h0 is None else torch.from_numpy(h0).cuda())
+    lib.check_device()
+    yr, sr = orc.ssd_fwd(inp["x"], inp["delta"], inp["A_log"], inp["B"], inp["C"], disc=disc, h0=h0)
+    return y.float().cpu().numpy(), fs.cpu().numpy(), yr, sr
+
+
+SHAPES = [(2, 200, 3, 32, 64), (1, 1000, 2, 64, 128), (2, 64, 1, 16, 128), (1, 7, 2, 16, 64), (1, 130, 1, 48, 128)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"b{s[0]}_L{s[1]}_H{s[2]}_P{s[3]}_N{s[4]}" for s in SHAPES])
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("with_h0", [False, True], ids=["zero_state", "h0"])
+def test_ssd_parity(orc, shape, disc, with_h0):
+    y, fs, yr, sr = _run(orc, *shape, disc, with_h0, seed=sum(shape))
+    ey, es = rel_err(y, yr), rel_err(fs, sr)
+    assert ey <= TOL["bf16"], f"y rel err {ey:.3g}"
+    assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
+
+
+def test_ssd_empty_sequence():
+    import torch
+    import selective_state_space_124_b300 as lib
+    batch, H, P, N = 2, 3, 16, 64
+    h0 = torch.randn((batch, H, P, N), device="cuda")
+    y, fs = lib.ssm_ssd_fwd(torch.zeros((batch, 0, H, P), dtype=torch.bfloat16, device="cuda"),
+                            torch.zeros((batch, 0, H), device="cuda"), torch.zeros(H, device="cuda"),
+                            torch.zeros((batch, 0, N), dtype=torch.bfloat16, device="cuda"),
+                            torch.zeros((batch, 0, N), dtype=torch.bfloat16, device="cuda"), h0=h0)
+    lib.check_device()
+    assert y.numel() == 0 and torch.equal(fs, h0)
+
+
+def test_ssd_mamba2_130m(orc):
+    """The full Mamba-2-130M-shaped layer (batch 2, L 2048, 24 heads x 64, N 128, Euler), every output."""
+    cfg = ssm_inputs.SSD_WORKLOADS["mamba2_130m"]
+    y, fs, yr, sr = _run(orc, cfg["batch"], cfg["L"], cfg["H"], cfg["P"], cfg["N"], cfg["disc"], False, seed=0)
+    ey, es = rel_err(y, yr), rel_err(fs, sr)
+    assert ey <= TOL["bf16"], f"y rel err {ey:.3g}"
+    assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
+
+
+def test_ssd_rejects_unsupported_shapes():
+    import torch
+    import selective_state_space_124_b300 as lib
+    x = torch.zeros((1, 8, 1, 16), dtype=torch.bfloat16, device="cuda")
+    Bm = torch.zeros((1, 8, 32), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lib.SsmError, match="N = 64 or 128"):
+        lib.ssm_ssd_fwd(x, torch.zeros((1, 8, 1), device="cuda"), torch.zeros(1, device="cuda"), Bm, Bm)
