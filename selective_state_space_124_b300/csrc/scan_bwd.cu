@@ -88,14 +88,39 @@ struct BwdChan {
   float invA[NP];  // 1 / A (ZOH), 0 where A == 0
 };
 
-// Abar - 1 and Bbar / B of one entry at one step.
+// e_n = Abar_n - 1 of every entry at one step. Generic A: one SFU exp2 (and the cancellation-free series)
+// per entry. Structured A (A_n = (n + 1) A_0, checked per piece): one exp2 for entry 0, then the exact identity
+// e_{m+k+1} = e_m (1 + e_k) + e_k gives the others with one FMA each (a tree four levels deep).
+template <int NP, bool ZOH, bool S4D>
+__device__ __forceinline__ void step_e(const BwdChan<NP, ZOH>& c, float dt, float (&e)[NP]) {
+  if constexpr (S4D) {
+    static_assert(NP == 16, "the structured path covers N = 16");
+    const float w = dt * c.A2[0];
+    e[0] = exp2m1(w, ex2(w));
+    e[1] = fmaf(e[0], 1.0f + e[0], e[0]);
+    const float a1 = 1.0f + e[1];
+    e[2] = fmaf(e[0], a1, e[1]);
+    e[3] = fmaf(e[1], a1, e[1]);
+    const float a3 = 1.0f + e[3];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) e[4 + k] = fmaf(e[k], a3, e[3]);
+    const float a7 = 1.0f + e[7];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) e[8 + k] = fmaf(e[k], a7, e[7]);
+  } else {
+#pragma unroll
+    for (int n = 0; n < NP; ++n) {
+      const float w = dt * c.A2[n];
+      e[n] = exp2m1(w, ex2(w));
+    }
+  }
+}
+
+// Bbar / B of entry n: delta (Euler), e_n / A_n (ZOH; delta where A_n == 0).
 template <int NP, bool ZOH>
-__device__ __forceinline__ void coefs(const BwdChan<NP, ZOH>& c, int n, float dt, float& a, float& e, float& bf) {
-  const float w = dt * c.A2[n];
-  a = ex2(w);
-  e = exp2m1(w, a);
-  if (ZOH) bf = c.A2[n] == 0.0f ? dt : e * c.invA[n];
-  else bf = dt;
+__device__ __forceinline__ float bfac(const BwdChan<NP, ZOH>& c, int n, float dt, float e) {
+  if (ZOH) return c.A2[n] == 0.0f ? dt : e * c.invA[n];
+  return dt;
 }
 
 // Sum over the warp of 32 values per lane (v[j], j < 32); lane l returns the total of v[l]. Recursive
@@ -156,6 +181,219 @@ __device__ __forceinline__ void load_chunk(const BwdParams& p, int64_t b, int64_
   __syncwarp();
 }
 
+// One piece [t0, t1) of a row (see the file comment for the four phases). S4D selects the structured-A
+// decay tree at compile time.
+template <int NP, bool ZOH, typename T, bool S4D>
+__device__ __forceinline__ void bwd_piece(const BwdParams& p, const BwdChan<NP, ZOH>& c, float* hs, float* xs,
+                                          float* ds, float* gs, float* bs, float* cs, int lane, int64_t row,
+                                          int64_t t0, int64_t t1) {
+  auto hrow = [&](int r, int n) -> float& { return hs[(r * NP + n) * 32 + lane]; };
+  constexpr int kStart = kChunk + 1;
+  const int N = static_cast<int>(p.N);
+  const int64_t L = p.L, D = p.D;
+  const int64_t b = row / p.groups;
+  const int64_t d = (row % p.groups) * 32 + lane;
+  const bool act = d < D;
+  // ---- 1. h(t0 - 1): walk back from t0 - 1 one chunk at a time ------------------------------------------
+  float h[NP];
+#pragma unroll
+  for (int n = 0; n < NP; ++n) h[n] = 0.0f;
+  const float* h0row = p.h0 ? p.h0 + (b * D + d) * N : nullptr;
+  if (t0 > 0) {
+    float P[NP];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) P[n] = 1.0f;
+    for (int64_t j = t0; j > 0;) {  // chunk [s, j)
+      const int64_t s = j > kChunk ? j - kChunk : 0;
+      const int cn = static_cast<int>(j - s);
+      load_chunk<T, true, false, true, false>(p, b, d, act, lane, s, cn, xs, ds, gs, bs, cs);
+#pragma unroll 1
+      for (int i = cn - 1; i >= 0; --i) {
+        const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
+        float ev[NP];
+        step_e<NP, ZOH, S4D>(c, dt, ev);
+#pragma unroll
+        for (int n = 0; n < NP; ++n) {
+          h[n] = fmaf(P[n], bfac(c, n, dt, ev[n]) * bs[i * 16 + n] * xv, h[n]);
+          P[n] = fmaf(P[n], ev[n], P[n]);
+        }
+      }
+      j = s;
+      float pm = 0.0f;
+#pragma unroll
+      for (int n = 0; n < NP; ++n) pm = fmaxf(pm, fabsf(P[n]));
+      if (!act) pm = 0.0f;
+      if (j > 0 && !__any_sync(0xffffffffu, pm >= kCarryEps)) break;
+      if (j == 0 && h0row && act) {  // the walk reached t = 0: exact, plus the decayed initial state
+#pragma unroll
+        for (int n = 0; n < NP; ++n)
+          if (n < N) h[n] = fmaf(P[n], h0row[n], h[n]);
+      }
+    }
+  } else if (h0row && act) {
+#pragma unroll
+    for (int n = 0; n < NP; ++n)
+      if (n < N) h[n] = h0row[n];
+  }
+#pragma unroll
+  for (int n = 0; n < NP; ++n) hrow(kStart, n) = h[n];
+
+  // ---- 2. forward over the piece in aligned chunks, saving the state at each chunk end followed by another
+  for (int64_t ck = t0 / kChunk; ck * kChunk < t1; ++ck) {
+    const int64_t s = ck * kChunk > t0 ? ck * kChunk : t0;
+    const int64_t e_ = (ck + 1) * kChunk < t1 ? (ck + 1) * kChunk : t1;
+    const int cn = static_cast<int>(e_ - s);
+    load_chunk<T, true, false, true, false>(p, b, d, act, lane, s, cn, xs, ds, gs, bs, cs);
+#pragma unroll 1
+    for (int i = 0; i < cn; ++i) {
+      const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
+      float ev[NP];
+      step_e<NP, ZOH, S4D>(c, dt, ev);
+#pragma unroll
+      for (int n = 0; n < NP; ++n) h[n] = fmaf(ev[n], h[n], h[n]) + bfac(c, n, dt, ev[n]) * bs[i * 16 + n] * xv;
+    }
+    if (e_ == (ck + 1) * kChunk && e_ < t1 && act) {  // chunk ck ends inside the piece
+      float* w = p.ws + ((b * p.nck + ck) * N) * D + d;
+#pragma unroll
+      for (int n = 0; n < NP; ++n)
+        if (n < N) w[static_cast<int64_t>(n) * D] = h[n];
+    }
+  }
+
+  // ---- 3. the adjoint entering from the right of the piece: walk forward from t1 one chunk at a time ----
+  float mu[NP];
+#pragma unroll
+  for (int n = 0; n < NP; ++n) mu[n] = 0.0f;
+  const float* dfrow = p.dfinal ? p.dfinal + (b * D + d) * N : nullptr;
+  if (t1 == L) {
+    if (dfrow && act) {
+#pragma unroll
+      for (int n = 0; n < NP; ++n)
+        if (n < N) mu[n] = dfrow[n];
+    }
+  } else {
+    float P[NP];
+#pragma unroll
+    for (int n = 0; n < NP; ++n) P[n] = 1.0f;
+    for (int64_t j = t1; j < L;) {  // chunk [j, e_)
+      const int64_t e_ = j + kChunk < L ? j + kChunk : L;
+      const int cn = static_cast<int>(e_ - j);
+      load_chunk<T, false, true, false, true>(p, b, d, act, lane, j, cn, xs, ds, gs, bs, cs);
+#pragma unroll 1
+      for (int i = 0; i < cn; ++i) {
+        const float dt = ds[i * 32 + lane], g = gs[i * 32 + lane];
+        float ev[NP];
+        step_e<NP, ZOH, S4D>(c, dt, ev);
+#pragma unroll
+        for (int n = 0; n < NP; ++n) {
+          P[n] = fmaf(P[n], ev[n], P[n]);
+          mu[n] = fmaf(P[n], cs[i * 16 + n] * g, mu[n]);
+        }
+      }
+      j = e_;
+      if (j == L) {  // exact: add the final-state gradient, decayed through every step after t1 - 1
+        if (dfrow && act) {
+#pragma unroll
+          for (int n = 0; n < NP; ++n)
+            if (n < N) mu[n] = fmaf(P[n], dfrow[n], mu[n]);
+        }
+        break;
+      }
+      float pm = 0.0f;
+#pragma unroll
+      for (int n = 0; n < NP; ++n) pm = fmaxf(pm, fabsf(P[n]));
+      if (!act) pm = 0.0f;
+      if (!__any_sync(0xffffffffu, pm >= kCarryEps)) break;
+    }
+  }
+
+  // ---- 4. chunks backwards ----------------------------------------------------------------------------
+  float dA[NP];
+#pragma unroll
+  for (int n = 0; n < NP; ++n) dA[n] = 0.0f;
+  for (int64_t ck = (t1 - 1) / kChunk; ck >= t0 / kChunk; --ck) {
+    const int64_t s = ck * kChunk > t0 ? ck * kChunk : t0;
+    const int64_t e_ = (ck + 1) * kChunk < t1 ? (ck + 1) * kChunk : t1;
+    const int cn = static_cast<int>(e_ - s);
+    load_chunk<T, true, true, true, true>(p, b, d, act, lane, s, cn, xs, ds, gs, bs, cs);
+    if (s == t0) {
+#pragma unroll
+      for (int n = 0; n < NP; ++n) h[n] = hrow(kStart, n);
+    } else {  // s = ck * kChunk > t0: chunk ck - 1 ends inside the piece; step 2 saved its state
+      const float* w = p.ws + ((b * p.nck + ck - 1) * N) * D + d;
+#pragma unroll
+      for (int n = 0; n < NP; ++n) h[n] = (act && n < N) ? w[static_cast<int64_t>(n) * D] : 0.0f;
+    }
+#pragma unroll
+    for (int n = 0; n < NP; ++n) hrow(0, n) = h[n];
+#pragma unroll 1
+    for (int i = 0; i < cn; ++i) {
+      const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
+      float ev[NP];
+      step_e<NP, ZOH, S4D>(c, dt, ev);
+#pragma unroll
+      for (int n = 0; n < NP; ++n) {
+        h[n] = fmaf(ev[n], h[n], h[n]) + bfac(c, n, dt, ev[n]) * bs[i * 16 + n] * xv;
+        hrow(i + 1, n) = h[n];
+      }
+    }
+#pragma unroll 1
+    for (int i = cn - 1; i >= 0; --i) {
+      const int64_t t = s + i;
+      const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane], g = gs[i * 32 + lane];
+      float gx = 0.0f, gdt = 0.0f;
+      float ev[NP];
+      step_e<NP, ZOH, S4D>(c, dt, ev);
+      float v[32];  // this lane's terms of dB (v[n]) and dC (v[16 + n]) at step t
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        v[n] = 0.0f;
+        v[16 + n] = 0.0f;
+      }
+#pragma unroll
+      for (int n = 0; n < NP; ++n) {
+        const float bn = bs[i * 16 + n], cn_ = cs[i * 16 + n];
+        const float e = ev[n], a = 1.0f + e, bf = bfac(c, n, dt, e);
+        const float An = c.A2[n] * kLn2;
+        const float lam = fmaf(cn_, g, mu[n]);
+        const float gb = lam * xv;           // dJ/dBbar
+        const float ga = lam * hrow(i, n);   // dJ/dAbar = lambda h_{t-1}
+        v[16 + n] = g * hrow(i + 1, n);      // dC term: dy h_t
+        v[n] = gb * bf;                      // dB term
+        gx = fmaf(lam * bf, bn, gx);
+        gdt = fmaf(ga * An, a, gdt);
+        dA[n] = fmaf(ga * dt, a, dA[n]);
+        if (ZOH) {
+          gdt = fmaf(gb * a, bn, gdt);
+          dA[n] = fmaf(gb * bn, dt * dt * zoh_dA_factor(dt * An, a, e), dA[n]);
+        } else {
+          gdt = fmaf(gb, bn, gdt);
+        }
+        mu[n] = a * lam;
+      }
+      if (act) {
+        const int64_t xi = (b * L + t) * D + d;
+        Elem<T>::store(p.dx, xi, gx);
+        Elem<T>::store(p.ddelta, xi, gdt);
+      }
+      const float tot = warp_reduce_scatter32(v, lane);  // lane l: total of v[l] over the warp
+      const int n_out = lane & 15;
+      if (n_out < N) atomicAdd((lane < 16 ? p.dB : p.dC) + (b * L + t) * N + n_out, tot);
+    }
+  }
+  if (act) {
+    if (t0 == 0 && p.dh0) {
+      float* out = p.dh0 + (b * D + d) * N;
+#pragma unroll
+      for (int n = 0; n < NP; ++n)
+        if (n < N) out[n] = mu[n];
+    }
+#pragma unroll
+    for (int n = 0; n < NP; ++n)
+      if (n < N) atomicAdd(p.dA_log + d * N + n, dA[n] * c.A2[n] * kLn2);
+  }
+}
+
 template <int NP, bool ZOH, typename T>
 __global__ void __launch_bounds__(kBwdWarps * 32, 1) scan_bwd_kernel(BwdParams p) {
   extern __shared__ float smem_bwd[];
@@ -171,8 +409,6 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) scan_bwd_kernel(BwdParams p
   float* gs = ds + kChunk * 32;
   float* bs = gs + kChunk * 32;
   float* cs = bs + kChunk * 16;
-  auto hrow = [&](int r, int n) -> float& { return hs[(r * NP + n) * 32 + lane]; };
-  constexpr int kStart = kChunk + 1;
 
   int64_t lo = static_cast<int64_t>(static_cast<__int128>(gw) * p.total / p.nwarps);
   const int64_t hi = static_cast<int64_t>(static_cast<__int128>(gw + 1) * p.total / p.nwarps);
@@ -183,218 +419,34 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) scan_bwd_kernel(BwdParams p
     const int64_t t0 = lo % L;
     const int64_t t1 = (hi - lo < L - t0) ? t0 + (hi - lo) : L;
     lo += t1 - t0;
-    const int64_t b = row / p.groups;
     const int64_t d = (row % p.groups) * 32 + lane;
     const bool act = d < D;
 
     BwdChan<NP, ZOH> c;
+    bool s4d = NP == 16 && N == 16;  // A[d, n] = (n + 1) A[d, 0] on every channel of the warp
 #pragma unroll
     for (int n = 0; n < NP; ++n) {
       float A = -1.0f;
-      if (act && n < N) A = -ex2(__ldg(p.A_log + d * N + n) * kLog2e);
+      if (act && n < N) A = -expf(__ldg(p.A_log + d * N + n));
       c.A2[n] = A * kLog2e;
       c.invA[n] = A == 0.0f ? 0.0f : 1.0f / A;
     }
-
-    // ---- 1. h(t0 - 1): walk back from t0 - 1 one chunk at a time ------------------------------------------
-    float h[NP];
-#pragma unroll
-    for (int n = 0; n < NP; ++n) h[n] = 0.0f;
-    const float* h0row = p.h0 ? p.h0 + (b * D + d) * N : nullptr;
-    if (t0 > 0) {
-      float P[NP];
-#pragma unroll
-      for (int n = 0; n < NP; ++n) P[n] = 1.0f;
-      for (int64_t j = t0; j > 0;) {  // chunk [s, j)
-        const int64_t s = j > kChunk ? j - kChunk : 0;
-        const int cn = static_cast<int>(j - s);
-        load_chunk<T, true, false, true, false>(p, b, d, act, lane, s, cn, xs, ds, gs, bs, cs);
-#pragma unroll 1
-        for (int i = cn - 1; i >= 0; --i) {
-          const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
-#pragma unroll
-          for (int n = 0; n < NP; ++n) {
-            float a, e, bf;
-            coefs<NP, ZOH>(c, n, dt, a, e, bf);
-            h[n] = fmaf(P[n], bf * bs[i * 16 + n] * xv, h[n]);
-            P[n] = fmaf(P[n], e, P[n]);
-          }
-        }
-        j = s;
-        float pm = 0.0f;
-#pragma unroll
-        for (int n = 0; n < NP; ++n) pm = fmaxf(pm, fabsf(P[n]));
-        if (!act) pm = 0.0f;
-        if (j > 0 && !__any_sync(0xffffffffu, pm >= kCarryEps)) break;
-        if (j == 0 && h0row && act) {  // the walk reached t = 0: exact, plus the decayed initial state
-#pragma unroll
-          for (int n = 0; n < NP; ++n)
-            if (n < N) h[n] = fmaf(P[n], h0row[n], h[n]);
-        }
-      }
-    } else if (h0row && act) {
-#pragma unroll
-      for (int n = 0; n < NP; ++n)
-        if (n < N) h[n] = h0row[n];
-    }
-#pragma unroll
-    for (int n = 0; n < NP; ++n) hrow(kStart, n) = h[n];
-
-    // ---- 2. forward over the piece in aligned chunks, saving the state at each chunk end followed by another
-    for (int64_t ck = t0 / kChunk; ck * kChunk < t1; ++ck) {
-      const int64_t s = ck * kChunk > t0 ? ck * kChunk : t0;
-      const int64_t e_ = (ck + 1) * kChunk < t1 ? (ck + 1) * kChunk : t1;
-      const int cn = static_cast<int>(e_ - s);
-      load_chunk<T, true, false, true, false>(p, b, d, act, lane, s, cn, xs, ds, gs, bs, cs);
-#pragma unroll 1
-      for (int i = 0; i < cn; ++i) {
-        const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
-#pragma unroll
-        for (int n = 0; n < NP; ++n) {
-          float a, e, bf;
-          coefs<NP, ZOH>(c, n, dt, a, e, bf);
-          h[n] = fmaf(e, h[n], h[n]) + bf * bs[i * 16 + n] * xv;
-        }
-      }
-      if (e_ == (ck + 1) * kChunk && e_ < t1 && act) {  // chunk ck ends inside the piece
-        float* w = p.ws + ((b * p.nck + ck) * N) * D + d;
-#pragma unroll
-        for (int n = 0; n < NP; ++n)
-          if (n < N) w[static_cast<int64_t>(n) * D] = h[n];
-      }
-    }
-
-    // ---- 3. the adjoint entering from the right of the piece: walk forward from t1 one chunk at a time ----
-    float mu[NP];
-#pragma unroll
-    for (int n = 0; n < NP; ++n) mu[n] = 0.0f;
-    const float* dfrow = p.dfinal ? p.dfinal + (b * D + d) * N : nullptr;
-    if (t1 == L) {
-      if (dfrow && act) {
-#pragma unroll
-        for (int n = 0; n < NP; ++n)
-          if (n < N) mu[n] = dfrow[n];
-      }
-    } else {
-      float P[NP];
-#pragma unroll
-      for (int n = 0; n < NP; ++n) P[n] = 1.0f;
-      for (int64_t j = t1; j < L;) {  // chunk [j, e_)
-        const int64_t e_ = j + kChunk < L ? j + kChunk : L;
-        const int cn = static_cast<int>(e_ - j);
-        load_chunk<T, false, true, false, true>(p, b, d, act, lane, j, cn, xs, ds, gs, bs, cs);
-#pragma unroll 1
-        for (int i = 0; i < cn; ++i) {
-          const float dt = ds[i * 32 + lane], g = gs[i * 32 + lane];
-#pragma unroll
-          for (int n = 0; n < NP; ++n) {
-            float a, e, bf;
-            coefs<NP, ZOH>(c, n, dt, a, e, bf);
-            P[n] = fmaf(P[n], e, P[n]);
-            mu[n] = fmaf(P[n], cs[i * 16 + n] * g, mu[n]);
-          }
-        }
-        j = e_;
-        if (j == L) {  // exact: add the final-state gradient, decayed through every step after t1 - 1
-          if (dfrow && act) {
-#pragma unroll
-            for (int n = 0; n < NP; ++n)
-              if (n < N) mu[n] = fmaf(P[n], dfrow[n], mu[n]);
-          }
-          break;
-        }
-        float pm = 0.0f;
-#pragma unroll
-        for (int n = 0; n < NP; ++n) pm = fmaxf(pm, fabsf(P[n]));
-        if (!act) pm = 0.0f;
-        if (!__any_sync(0xffffffffu, pm >= kCarryEps)) break;
-      }
-    }
-
-    // ---- 4. chunks backwards ----------------------------------------------------------------------------
-    float dA[NP];
-#pragma unroll
-    for (int n = 0; n < NP; ++n) dA[n] = 0.0f;
-    for (int64_t ck = (t1 - 1) / kChunk; ck >= t0 / kChunk; --ck) {
-      const int64_t s = ck * kChunk > t0 ? ck * kChunk : t0;
-      const int64_t e_ = (ck + 1) * kChunk < t1 ? (ck + 1) * kChunk : t1;
-      const int cn = static_cast<int>(e_ - s);
-      load_chunk<T, true, true, true, true>(p, b, d, act, lane, s, cn, xs, ds, gs, bs, cs);
-      if (s == t0) {
-#pragma unroll
-        for (int n = 0; n < NP; ++n) h[n] = hrow(kStart, n);
-      } else {  // s = ck * kChunk > t0: chunk ck - 1 ends inside the piece; step 2 saved its state
-        const float* w = p.ws + ((b * p.nck + ck - 1) * N) * D + d;
-#pragma unroll
-        for (int n = 0; n < NP; ++n) h[n] = (act && n < N) ? w[static_cast<int64_t>(n) * D] : 0.0f;
-      }
-#pragma unroll
-      for (int n = 0; n < NP; ++n) hrow(0, n) = h[n];
-#pragma unroll 1
-      for (int i = 0; i < cn; ++i) {
-        const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
-#pragma unroll
-        for (int n = 0; n < NP; ++n) {
-          float a, e, bf;
-          coefs<NP, ZOH>(c, n, dt, a, e, bf);
-          h[n] = fmaf(e, h[n], h[n]) + bf * bs[i * 16 + n] * xv;
-          hrow(i + 1, n) = h[n];
-        }
-      }
-#pragma unroll 1
-      for (int i = cn - 1; i >= 0; --i) {
-        const int64_t t = s + i;
-        const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane], g = gs[i * 32 + lane];
-        float gx = 0.0f, gdt = 0.0f;
-        float v[32];  // this lane's terms of dB (v[n]) and dC (v[16 + n]) at step t
-#pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          v[n] = 0.0f;
-          v[16 + n] = 0.0f;
-        }
-#pragma unroll
-        for (int n = 0; n < NP; ++n) {
-          const float bn = bs[i * 16 + n], cn_ = cs[i * 16 + n];
-          float a, e, bf;
-          coefs<NP, ZOH>(c, n, dt, a, e, bf);
-          const float An = c.A2[n] * kLn2;
-          const float lam = fmaf(cn_, g, mu[n]);
-          const float gb = lam * xv;           // dJ/dBbar
-          const float ga = lam * hrow(i, n);   // dJ/dAbar = lambda h_{t-1}
-          v[16 + n] = g * hrow(i + 1, n);      // dC term: dy h_t
-          v[n] = gb * bf;                      // dB term
-          gx = fmaf(lam * bf, bn, gx);
-          gdt = fmaf(ga * An, a, gdt);
-          dA[n] = fmaf(ga * dt, a, dA[n]);
-          if (ZOH) {
-            gdt = fmaf(gb * a, bn, gdt);
-            dA[n] = fmaf(gb * bn, dt * dt * zoh_dA_factor(dt * An, a, e), dA[n]);
-          } else {
-            gdt = fmaf(gb, bn, gdt);
-          }
-          mu[n] = a * lam;
-        }
-        if (act) {
-          const int64_t xi = (b * L + t) * D + d;
-          Elem<T>::store(p.dx, xi, gx);
-          Elem<T>::store(p.ddelta, xi, gdt);
-        }
-        const float tot = warp_reduce_scatter32(v, lane);  // lane l: total of v[l] over the warp
-        const int n_out = lane & 15;
-        if (n_out < N) atomicAdd((lane < 16 ? p.dB : p.dC) + (b * L + t) * N + n_out, tot);
-      }
-    }
     if (act) {
-      if (t0 == 0 && p.dh0) {
-        float* out = p.dh0 + (b * D + d) * N;
+      const float A0 = c.A2[0] / kLog2e;
+      s4d = s4d && A0 < -1e-30f && A0 > -3.0e38f;
 #pragma unroll
-        for (int n = 0; n < NP; ++n)
-          if (n < N) out[n] = mu[n];
+      for (int n = 1; n < NP; ++n) {
+        const float A = -expf(__ldg(p.A_log + d * N + (n < N ? n : 0)));
+        s4d = s4d && fabsf(A - static_cast<float>(n + 1) * A0) <= 4.8e-7f * fabsf(A);
       }
-#pragma unroll
-      for (int n = 0; n < NP; ++n)
-        if (n < N) atomicAdd(p.dA_log + d * N + n, dA[n] * c.A2[n] * kLn2);
     }
+    if constexpr (NP == 16) {
+      if (__all_sync(0xffffffffu, s4d)) {
+        bwd_piece<NP, ZOH, T, true>(p, c, hs, xs, ds, gs, bs, cs, lane, row, t0, t1);
+        continue;
+      }
+    }
+    bwd_piece<NP, ZOH, T, false>(p, c, hs, xs, ds, gs, bs, cs, lane, row, t0, t1);
   }
 }
 

@@ -94,12 +94,12 @@ struct SsdSmem {
   alignas(128) __nv_bfloat16 Bt[2][kQ * N];
   alignas(128) __nv_bfloat16 Ct[2][kQ * N];
   alignas(128) __nv_bfloat16 Xt[2][kQ * kPB];
-  alignas(128) __nv_bfloat16 Xw[kQ * kPB];  // w_j x_j, the state update's operand
   alignas(128) __nv_bfloat16 Sb[N * kPB];   // bf16 copy of the state slice [N][16]
   float dt[2][kQ];
-  float s[kQ];                              // log decay from the chunk start through step i
-  float coef[kQ];
-  float w[kQ];                              // e^{s_last - s_j} coef_j
+  // per warp (each warp forms its own copy, so no barrier separates them from their use):
+  float s[kThreads / 32][kQ];               // log decay from the chunk start through step i
+  float coef[kThreads / 32][kQ];
+  float w[kThreads / 32][kQ];               // e^{s_last - s_j} coef_j
 };
 
 template <int N>
@@ -186,8 +186,11 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
     }
     __syncthreads();  // chunk c's tiles, dt and the state copy are visible to every warp
 
-    // ---- running log decay, input coefficients and state-update weights (warp 0) ---------------------
-    if (warp == 0) {
+    // ---- running log decay, input coefficients and state-update weights (every warp its own copy) -----
+    float* const sw = sm.s[warp];
+    float* const cw = sm.coef[warp];
+    float* const ww = sm.w[warp];
+    {
       const float d0 = sm.dt[buf][2 * lane], d1 = sm.dt[buf][2 * lane + 1];
       float v0 = d0 * A, v1 = v0 + d1 * A;  // inclusive sums within the lane's pair
       float inc = v1;
@@ -207,29 +210,18 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
         return A == 0.0f ? d : e / A;
       };
       const float c0 = coef_of(d0), c1 = coef_of(d1);
-      sm.s[2 * lane] = s0;
-      sm.s[2 * lane + 1] = s1;
-      sm.coef[2 * lane] = c0;
-      sm.coef[2 * lane + 1] = c1;
-      sm.w[2 * lane] = ex2((last - s0) * kLog2e) * c0;
-      sm.w[2 * lane + 1] = ex2((last - s1) * kLog2e) * c1;
+      sw[2 * lane] = s0;
+      sw[2 * lane + 1] = s1;
+      cw[2 * lane] = c0;
+      cw[2 * lane + 1] = c1;
+      ww[2 * lane] = ex2((last - s0) * kLog2e) * c0;
+      ww[2 * lane + 1] = ex2((last - s1) * kLog2e) * c1;
     }
-    __syncthreads();
-    const float s_last = sm.s[kQ - 1];
-    // scaled x for the state update: Xw[j][p] = w_j x[j][p] (bf16)
-#pragma unroll
-    for (int k = tid; k < kQ * kPB / 2; k += kThreads) {
-      const int row = k / (kPB / 2), col = (k % (kPB / 2)) * 2;
-      const uint32_t off = p16_off(row, col >> 3) + (col & 7) * 2;
-      const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(reinterpret_cast<const char*>(sm.Xt[buf]) + off);
-      const float wj = sm.w[row];
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(sm.Xw) + off) =
-          pack_bf16(__low2float(v) * wj, __high2float(v) * wj);
-    }
-    __syncthreads();
+    __syncwarp();
+    const float s_last = sw[kQ - 1];
 
     const uint32_t Cb = smem_u32(sm.Ct[buf]), Bb = smem_u32(sm.Bt[buf]), Xb = smem_u32(sm.Xt[buf]);
-    const uint32_t Sbb = smem_u32(sm.Sb), Xwb = smem_u32(sm.Xw);
+    const uint32_t Sbb = smem_u32(sm.Sb);
     const int mi = lane >> 3, r8 = lane & 7;  // ldmatrix: which 8x8 matrix this lane addresses, and its row
 
     // ---- G = C B^T for this warp's 16 rows (causal column tiles only) --------------------------------
@@ -258,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
     }
     // mask and scale: G'[i][j] = G[i][j] e^{s_i - s_j} coef_j for j <= i, else 0
     const int i_lo = warp * 16 + (lane >> 2), i_hi = i_lo + 8;
-    const float si_lo = sm.s[i_lo], si_hi = sm.s[i_hi];
+    const float si_lo = sw[i_lo], si_hi = sw[i_hi];
     uint32_t ga[4][4];  // G' as the A operand of Y1 (k = j)
 #pragma unroll
     for (int np = 0; np < 4; ++np) {
@@ -270,7 +262,7 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
           const int j = (2 * np + q) * 8 + 2 * (lane & 3) + (r & 1);
           const int i = (r & 2) ? i_hi : i_lo;
           const float si = (r & 2) ? si_hi : si_lo;
-          v[q][r] = (np <= warp && j <= i) ? g[2 * np + q][r] * ex2((si - sm.s[j]) * kLog2e) * sm.coef[j] : 0.0f;
+          v[q][r] = (np <= warp && j <= i) ? g[2 * np + q][r] * ex2((si - sw[j]) * kLog2e) * cw[j] : 0.0f;
         }
       ga[np][0] = pack_bf16(v[0][0], v[0][1]);
       ga[np][1] = pack_bf16(v[0][2], v[0][3]);
@@ -331,7 +323,20 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
       for (int kk = 0; kk < kQ / 16; ++kk) {
         uint32_t b0, b1, b2, b3;
         const int xrow = kk * 16 + (mi & 1) * 8 + r8;
-        ldsm_x4_t(Xwb + p16_off(xrow, mi >> 1), b0, b1, b2, b3);
+        ldsm_x4_t(Xb + p16_off(xrow, mi >> 1), b0, b1, b2, b3);
+        {  // scale row k of x by w_k in registers: b0, b2 hold rows k0, k0 + 1; b1, b3 rows k0 + 8, k0 + 9
+          const int k0 = kk * 16 + 2 * (lane & 3);
+          const float2 wa = *reinterpret_cast<const float2*>(ww + k0);
+          const float2 wb = *reinterpret_cast<const float2*>(ww + k0 + 8);
+          auto scale = [](uint32_t v, float2 f) {
+            const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&v);
+            return pack_bf16(__low2float(x) * f.x, __high2float(x) * f.y);
+          };
+          b0 = scale(b0, wa);
+          b2 = scale(b2, wa);
+          b1 = scale(b1, wb);
+          b3 = scale(b3, wb);
+        }
 #pragma unroll
         for (int mt = 0; mt < kMT; ++mt) {
           // A = B^T: rows n (this warp's), k = j; the transposed load of B rows j gives it

@@ -36,9 +36,9 @@ def _dy(rng, shape, dtype):
     return dy
 
 
-def _run(orc, batch, L, D, N, disc, dtype, with_state, seed, mu=-2.0):
+def _run(orc, batch, L, D, N, disc, dtype, with_state, seed, mu=-2.0, a_log=None):
     import selective_state_space_124_b300 as lib
-    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=seed, dtype=dtype, mu=mu)
+    inp = ssm_inputs.make_inputs(batch, L, D, N, seed=seed, dtype=dtype, mu=mu, a_log=a_log)
     rng = np.random.default_rng(seed + 1)
     dy = _dy(rng, (batch, L, D), dtype)
     h0 = rng.standard_normal((batch, D, N)).astype(np.float32) if with_state else None
@@ -65,6 +65,19 @@ def test_bwd_parity(orc, shape, disc, dtype, with_state):
     for k in KEYS:
         e = rel_err(got[k], ref[k])
         assert e <= TOL[dtype], f"{k} rel err {e:.3g}"
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_bwd_unstructured_A(orc, disc):
+    """N = 16 with A_log drawn at random (no A_n = (n + 1) A_0 structure), one structured warp group and one
+    not: the per-entry path and the decay-tree path in one launch."""
+    batch, L, D, N = 2, 600, 64, 16
+    a_log = np.tile(np.log(np.arange(1, N + 1, dtype=np.float32)), (D, 1))
+    a_log[32:] = np.random.default_rng(3).uniform(-1.0, 1.5, (D - 32, N)).astype(np.float32)
+    got, ref = _run(orc, batch, L, D, N, disc, "f32", True, seed=9, a_log=a_log)
+    for k in KEYS:
+        e = rel_err(got[k], ref[k])
+        assert e <= TOL["f32"], f"{k} rel err {e:.3g}"
 
 
 def test_bwd_long_memory(orc):
