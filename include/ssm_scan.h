@@ -19,8 +19,9 @@
  * itself uses"). delta is taken as given (already made positive upstream; no softplus inside).
  *
  * Conventions shared by every entry point:
- *  - Every pointer is DEVICE memory of the current CUDA device, owned by the caller. The library
- *    allocates nothing, frees nothing and keeps no pointer after a call returns.
+ *  - Every pointer is DEVICE memory of the current CUDA device, owned by the caller. No call allocates or
+ *    frees memory, and none keeps a pointer after it returns. The one exception: ssm_scan_bwd_noalloc
+ *    uses a fixed 64 MiB scratch array, which every device that loads the library reserves at load time.
  *  - Layouts are dense row-major in the shapes given. "dtype" arrays hold fp32 (SSM_DTYPE_F32) or
  *    bf16 (SSM_DTYPE_BF16) elements; A_log, states, h0 and final_state are always fp32.
  *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy default
