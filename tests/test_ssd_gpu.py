@@ -31,7 +31,9 @@ def _run(orc, batch, L, H, P, N, disc, with_h0, seed):
     return y.float().cpu().numpy(), fs.cpu().numpy(), yr, sr
 
 
-SHAPES = [(2, 200, 3, 32, 64), (1, 1000, 2, 64, 128), (2, 64, 1, 16, 128), (1, 7, 2, 16, 64), (1, 130, 1, 48, 128)]
+# the last shape has 24 heads (384 CTAs: more than two per SM)
+SHAPES = [(2, 200, 3, 32, 64), (1, 1000, 2, 64, 128), (2, 64, 1, 16, 128), (1, 7, 2, 16, 64), (1, 130, 1, 48, 128),
+          (4, 130, 24, 64, 64)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"b{s[0]}_L{s[1]}_H{s[2]}_P{s[3]}_N{s[4]}" for s in SHAPES])
