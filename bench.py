@@ -373,11 +373,13 @@ def measure_ssd(name, reps, flush, peak):
     y = torch.empty((b, L, H, P), dtype=torch.bfloat16, device="cuda")
     fs = torch.empty((b, H, P, N), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
-    args = [t.data_ptr() for t in (x, dt, A, B, C)] + [0, y.data_ptr(), fs.data_ptr()]
+    need = lib.ssd_workspace_size(b, L, H, P, N)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    args = [t.data_ptr() for t in (x, dt, A, B, C)] + [0, y.data_ptr(), fs.data_ptr(), ws.data_ptr()]
     from selective_state_space_124_b300 import _ffi
     fn = _ffi.load().ssm_ssd_fwd
     import ctypes
-    cargs = [ctypes.c_void_p(a) if a else None for a in args] + [b, L, H, P, N, _ffi.DTYPE["bf16"],
+    cargs = [ctypes.c_void_p(a) if a else None for a in args] + [need, b, L, H, P, N, _ffi.DTYPE["bf16"],
                                                                  _ffi.DISC[cfg["disc"]], ctypes.c_void_p(stream.cuda_stream)]
     ms = []
     for i in range(3 + reps):
@@ -397,7 +399,7 @@ def measure_ssd(name, reps, flush, peak):
                         f"chunks of 64", "launch_ms_median": med * 1e3, "elems_per_s": b * L * H * P / med,
             "gbs": nbytes / med / 1e9, "hbm_frac": nbytes / med / 1e9 / peak, "bytes_per_launch": nbytes,
             "tflops": flops / med / 1e12, "tensor_frac": flops / med / 1e12 / bf16_peak if bf16_peak else None,
-            "flops_per_launch": flops, "reps": reps}
+            "flops_per_launch": flops, "workspace_bytes": need, "reps": reps}
 
 
 def measure_decode(steps, flush, peak):

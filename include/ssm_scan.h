@@ -188,15 +188,24 @@ ssm_status ssm_scan_bwd_noalloc(const void *x, const void *delta, const float *A
  *   B, C        [batch, L, N]     bf16, one group shared by every head
  *   h0          [batch, H, P, N]  fp32 initial state, or NULL
  *   final_state [batch, H, P, N]  fp32, or NULL
+ *   workspace   device memory of ssm_ssd_fwd_workspace_size() bytes, or NULL. With it, each sequence is
+ *               cut into segments that separate CTAs scan from a zero state, and a second pass adds the
+ *               state carried into each segment. Without it (or when it is too small), one CTA walks each
+ *               sequence. Both give the same function. Its contents on entry do not matter. Two calls in
+ *               flight may not share it.
  * N must be 64 or 128 and P a multiple of 16 (else SSM_ERR_UNSUPPORTED); x, B, C and y must be 16-byte
  * aligned (else SSM_ERR_UNSUPPORTED). The products run with bf16 operands and fp32 accumulation (the
  * masked score tile and a bf16 copy of the carried state are rounded to bf16 as operands; the state itself
  * is carried in fp32). Other conventions as for ssm_scan_fwd.
  */
 ssm_status ssm_ssd_fwd(const void *x, const float *delta, const float *A_log, const void *B, const void *C,
-                       const float *h0, void *y, float *final_state,
+                       const float *h0, void *y, float *final_state, void *workspace, size_t workspace_bytes,
                        int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N,
                        ssm_dtype dtype, ssm_disc disc, void *stream);
+
+/* Bytes of workspace that let ssm_ssd_fwd cut long sequences into segments scanned in parallel (on the current
+   device; 0 when one CTA per sequence already fills it, or for unsupported shapes). */
+size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N);
 
 /* Synchronise `stream` and report any error raised while this library's kernels ran on it. */
 ssm_status ssm_check_device(void *stream);

@@ -21,7 +21,7 @@ from . import _ffi
 from ._ffi import SsmError
 
 __all__ = ["ssm_scan_fwd", "ssm_scan_step", "ssm_scan_bwd", "ssm_scan_fwd_ptr", "ssm_scan_step_ptr",
-           "bwd_workspace_size", "ssm_ssd_fwd", "check_device", "SsmError", "version"]
+           "bwd_workspace_size", "ssm_ssd_fwd", "ssd_workspace_size", "check_device", "SsmError", "version"]
 
 
 def _torch():
@@ -206,10 +206,17 @@ def ssm_scan_bwd(x, delta, A_log, B, C, dy, disc: str = "euler", h0=None, dfinal
     return out
 
 
-def ssm_ssd_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, want_final_state: bool = True, stream=None):
+def ssd_workspace_size(batch: int, L: int, H: int, P: int, N: int) -> int:
+    """Bytes of workspace that let ssm_ssd_fwd scan segments of each sequence in parallel (current device)."""
+    return int(_ffi.load().ssm_ssd_fwd_workspace_size(batch, L, H, P, N))
+
+
+def ssm_ssd_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, want_final_state: bool = True, stream=None,
+                workspace="auto"):
     """Mamba-2 SSD layer (scalar A per head), CUDA tensors: x [batch, L, H, P] bf16, delta [batch, L, H]
     float32, A_log [H] float32, B, C [batch, L, N] bf16, h0 [batch, H, P, N] float32 or None. Returns
-    (y [batch, L, H, P] bf16, final_state [batch, H, P, N] float32 or None)."""
+    (y [batch, L, H, P] bf16, final_state [batch, H, P, N] float32 or None). ``workspace``: "auto" allocates
+    the segment workspace here, None runs one CTA per sequence, or a uint8 CUDA tensor."""
     torch = _torch()
     batch, L, H, P = x.shape
     N = B.shape[-1]
@@ -225,9 +232,14 @@ def ssm_ssd_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, want_fin
         raise ValueError("inputs must be contiguous CUDA tensors on one device")
     y = torch.empty((batch, L, H, P), dtype=torch.bfloat16, device=x.device)
     fs = torch.empty((batch, H, P, N), dtype=torch.float32, device=x.device) if want_final_state else None
+    if isinstance(workspace, str):
+        need = ssd_workspace_size(batch, L, H, P, N)
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device) if need > 0 else None
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     s = stream if stream is not None else torch.cuda.current_stream(x.device)
     st = _ffi.load().ssm_ssd_fwd(_ptr(x), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(h0), _ptr(y), _ptr(fs),
-                                 batch, L, H, P, N, _ffi.DTYPE["bf16"], _ffi.DISC[disc], ctypes_void(s.cuda_stream))
+                                 _ptr(workspace), wbytes, batch, L, H, P, N, _ffi.DTYPE["bf16"], _ffi.DISC[disc],
+                                 ctypes_void(s.cuda_stream))
     _ffi.check("ssm_ssd_fwd", st)
     return y, fs
 

@@ -28,7 +28,9 @@ SIGNATURES = {
     "ssm_scan_bwd_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i64]),
     "ssm_scan_bwd_noalloc": (_i32, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _vp, _vp, _fp, _fp, _fp, _fp,
                                     _i64, _i64, _i64, _i64, _i32, _i32, _vp]),
-    "ssm_ssd_fwd": (_i32, [_vp, _fp, _fp, _vp, _vp, _fp, _vp, _fp, _i64, _i64, _i64, _i64, _i64, _i32, _i32, _vp]),
+    "ssm_ssd_fwd": (_i32, [_vp, _fp, _fp, _vp, _vp, _fp, _vp, _fp, _vp, ctypes.c_size_t, _i64, _i64, _i64, _i64, _i64,
+                           _i32, _i32, _vp]),
+    "ssm_ssd_fwd_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i64, _i64]),
     "ssm_check_device": (_i32, [_vp]),
     "ssm_status_string": (ctypes.c_char_p, [_i32]),
     "ssm_last_error": (ctypes.c_char_p, []),

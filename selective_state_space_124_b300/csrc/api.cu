@@ -220,9 +220,16 @@ ssm_status ssm_scan_bwd_noalloc(const void* x, const void* delta, const float* A
                       kBwdNoAllocScratchBytes, batch, L, D, N, dtype, disc, stream);
 }
 
+size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N) {
+  int64_t bl = 0, blh = 0, blhp = 0;
+  if (!ssd_shape_ok(P, N) || !mul_ok(batch, L, &bl) || !mul_ok(bl, H, &blh) || !mul_ok(blh, P, &blhp)) return 0;
+  return ssd_workspace_bytes(batch, L, H, P, N);
+}
+
 ssm_status ssm_ssd_fwd(const void* x, const float* delta, const float* A_log, const void* B, const void* C,
-                       const float* h0, void* y, float* final_state, int64_t batch, int64_t L, int64_t H, int64_t P,
-                       int64_t N, ssm_dtype dtype, ssm_disc disc, void* stream) {
+                       const float* h0, void* y, float* final_state, void* workspace, size_t workspace_bytes,
+                       int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N, ssm_dtype dtype, ssm_disc disc,
+                       void* stream) {
   g_last_error[0] = '\0';
   if (!valid_enums(dtype, disc)) return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: bad dtype or disc");
   if (batch < 0 || L < 0 || H < 0 || P < 1 || N < 1)
@@ -245,14 +252,17 @@ ssm_status ssm_ssd_fwd(const void* x, const float* delta, const float* A_log, co
   if (mis & 15) return fail(SSM_ERR_UNSUPPORTED, "ssm_ssd_fwd: x, B, C and y must be 16-byte aligned");
   const Range ry = range_of(y, blhp, 2);
   const Range rf = range_of(final_state, final_state ? bhpn : 0, 4);
+  const Range rw = range_of(workspace, workspace ? static_cast<int64_t>(workspace_bytes) : 0, 1);
   const Range ins[] = {range_of(x, blhp, 2), range_of(delta, blh, 4), range_of(A_log, H, 4), range_of(B, bln, 2),
                        range_of(C, bln, 2), range_of(h0, h0 ? bhpn : 0, 4)};
   for (const Range& r : ins)
-    if (overlap(ry, r) || overlap(rf, r)) return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: outputs overlap inputs");
-  if (overlap(ry, rf)) return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: y overlaps final_state");
+    if (overlap(ry, r) || overlap(rf, r) || overlap(rw, r))
+      return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: outputs or workspace overlap inputs");
+  if (overlap(ry, rf) || overlap(rw, ry) || overlap(rw, rf))
+    return fail(SSM_ERR_INVALID_ARG, "ssm_ssd_fwd: y, final_state and workspace overlap");
   if (bh == 0) return SSM_OK;
-  SsdArgs a{x, delta, A_log, B, C, h0, y, final_state, batch, L, H, P, N, static_cast<int>(disc),
-            static_cast<cudaStream_t>(stream)};
+  SsdArgs a{x, delta, A_log, B, C, h0, y, final_state, workspace, workspace_bytes, batch, L, H, P, N,
+            static_cast<int>(disc), static_cast<cudaStream_t>(stream)};
   cudaError_t e = launch_ssd(a);
   if (e != cudaSuccess) return cuda_fail(e, "ssm_ssd_fwd launch");
   return SSM_OK;

@@ -74,6 +74,8 @@ struct SsdArgs {
   const float* h0;      // [batch, H, P, N] or null
   void* y;              // [batch, L, H, P] bf16
   float* final_state;   // [batch, H, P, N] or null
+  void* workspace;      // ssd_workspace_bytes() bytes for the segmented scan, or null (one CTA per sequence)
+  size_t workspace_bytes;
   int64_t batch, L, H, P, N;
   int disc;
   cudaStream_t stream;
@@ -92,6 +94,7 @@ constexpr size_t kBwdNoAllocScratchBytes = size_t(64) << 20;  // the built-in sc
 cudaError_t bwd_noalloc_scratch(void** out);                     // its device address on the current device
 cudaError_t launch_bwd(const BwdArgs& a);
 bool ssd_shape_ok(int64_t P, int64_t N);  // N in {64, 128}, P a multiple of 16
+size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N);  // current device
 cudaError_t launch_ssd(const SsdArgs& a);
 
 }  // namespace ssm

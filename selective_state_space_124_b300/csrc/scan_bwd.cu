@@ -454,8 +454,15 @@ template <int NP, bool ZOH, typename T>
 cudaError_t launch_bwd_np(const BwdParams& bp, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(kBwdWarps) * kBwdWarpFloats<NP> * sizeof(float);
   auto kern = scan_bwd_kernel<NP, ZOH, T>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static bool attr_set[64] = {false};  // per device, once per instantiation
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (!attr_set[dev & 63]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev & 63] = true;
+  }
   const int64_t blocks = (bp.nwarps + kBwdWarps - 1) / kBwdWarps;
   kern<<<static_cast<unsigned>(blocks), kBwdWarps * 32, smem, s>>>(bp);
   return cudaGetLastError();

@@ -42,6 +42,13 @@ struct SsdParams {
   float* final_state;      // [batch, H, P, N] or null
   int64_t batch, L, H, P;
   int pblocks;             // P / kPB
+  // segments: each (batch element, head) sequence is cut into nseg runs of cps chunks, scanned by separate CTAs
+  // from a zero state (segment 0 from h0); seg_state / seg_logdec receive each segment's end state and total
+  // log decay for the fix-up pass. nseg == 1: one CTA walks the whole sequence and writes final_state itself.
+  int nseg;
+  int64_t cps;
+  float* seg_state;        // [batch, H, nseg, P, N] or null (nseg == 1)
+  float* seg_logdec;       // [batch, H, nseg]
 };
 
 // ---- PTX wrappers ------------------------------------------------------------------------------------
@@ -131,8 +138,9 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   SsdSmem<N>& sm = *reinterpret_cast<SsdSmem<N>*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t bh = blockIdx.x / p.pblocks;
   const int p0 = (blockIdx.x % p.pblocks) * kPB;
+  const int seg = static_cast<int>((blockIdx.x / p.pblocks) % p.nseg);
+  const int64_t bh = blockIdx.x / p.pblocks / p.nseg;
   const int64_t b = bh / p.H, h = bh % p.H;
   const int64_t L = p.L;
   const float A = -ex2(__ldg(p.A_log + h) * kLog2e);
@@ -151,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
       for (int r = 0; r < 4; ++r) {
         const int n = warp * kNW + mt * 16 + (lane >> 2) + ((r & 2) ? 8 : 0);
         const int pp = p0 + nt * 8 + 2 * (lane & 3) + (r & 1);
-        st[mt][nt][r] = p.h0 ? p.h0[((b * p.H + h) * p.P + pp) * N + n] : 0.0f;
+        st[mt][nt][r] = (p.h0 && seg == 0) ? p.h0[((b * p.H + h) * p.P + pp) * N + n] : 0.0f;
       }
   auto write_state_copy = [&]() {
 #pragma unroll
@@ -168,13 +176,16 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
   };
   write_state_copy();
 
-  const int64_t nchunks = (L + kQ - 1) / kQ;
-  if (nchunks > 0) load_chunk<N>(p, sm, 0, b, h, p0, 0, tid);
-  float dt_next = (tid < kQ && tid < L) ? p.delta[(b * L + tid) * p.H + h] : 0.0f;
+  const int64_t nchunks_all = (L + kQ - 1) / kQ;
+  const int64_t cbeg = seg * p.cps;
+  const int64_t nchunks = cbeg + p.cps < nchunks_all ? cbeg + p.cps : nchunks_all;  // this segment's end chunk
+  if (cbeg < nchunks) load_chunk<N>(p, sm, 0, b, h, p0, cbeg * kQ, tid);
+  float dt_next = (tid < kQ && cbeg * kQ + tid < L) ? p.delta[(b * L + cbeg * kQ + tid) * p.H + h] : 0.0f;
   if (tid < kQ) sm.dt[0][tid] = dt_next;
+  float logdec = 0.0f;  // the segment's total log decay (sum of delta A)
 
-  for (int64_t c = 0; c < nchunks; ++c) {
-    const int buf = static_cast<int>(c & 1);
+  for (int64_t c = cbeg; c < nchunks; ++c) {
+    const int buf = static_cast<int>((c - cbeg) & 1);
     const int64_t t0 = c * kQ;
     if (c + 1 < nchunks) {  // the other buffer's last readers finished before the previous chunk's barrier
       load_chunk<N>(p, sm, buf ^ 1, b, h, p0, t0 + kQ, tid);
@@ -219,6 +230,7 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
     }
     __syncwarp();
     const float s_last = sw[kQ - 1];
+    logdec += s_last;
 
     const uint32_t Cb = smem_u32(sm.Ct[buf]), Bb = smem_u32(sm.Bt[buf]), Xb = smem_u32(sm.Xt[buf]);
     const uint32_t Sbb = smem_u32(sm.Sb);
@@ -353,7 +365,9 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
     write_state_copy();
     if (tid < kQ) sm.dt[buf ^ 1][tid] = dt_next;
   }
-  if (p.final_state) {
+  float* const out = p.nseg > 1 ? p.seg_state + (bh * p.nseg + seg) * p.P * N
+                                 : (p.final_state ? p.final_state + bh * p.P * N : nullptr);
+  if (out) {
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
@@ -362,25 +376,208 @@ __global__ void __launch_bounds__(kThreads) ssd_fwd_kernel(SsdParams p) {
         for (int r = 0; r < 4; ++r) {
           const int n = warp * kNW + mt * 16 + (lane >> 2) + ((r & 2) ? 8 : 0);
           const int pp = p0 + nt * 8 + 2 * (lane & 3) + (r & 1);
-          p.final_state[((b * p.H + h) * p.P + pp) * N + n] = st[mt][nt][r];
+          out[static_cast<int64_t>(pp) * N + n] = st[mt][nt][r];
         }
   }
+  if (p.nseg > 1 && p0 == 0 && tid == 0) p.seg_logdec[bh * p.nseg + seg] = logdec;
+}
+
+// Fix-up of segments 1 .. nseg-1 (one CTA per batch element, head, segment, chunk of the segment and 16-channel
+// block, so every chunk is corrected in parallel). The state
+// entering segment s is H_s = E_{s-1} + e^{D_{s-1}} H_{s-1}, H_1 = E_0 (E_u, D_u: segment u's end state from a
+// zero start and its total log decay; segment 0 started from h0). Its contribution to every output of the
+// segment is e^{cum_i} C_i . H_s, cum_i the log decay from the segment start through step i: a product with the
+// C rows, added to the y the first pass wrote. The last segment's first-chunk CTA also writes the final state
+// E_last + e^{D_last} H_last.
+template <int N>
+struct FixSmem {
+  alignas(128) __nv_bfloat16 Ct[kQ * N];
+  alignas(128) __nv_bfloat16 Sb[N * kPB];
+  float dt[kQ];
+  float cum[kQ];
+  float part[kThreads / 32];
+};
+
+template <int N>
+__global__ void __launch_bounds__(kThreads) ssd_fixup_kernel(SsdParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  FixSmem<N>& sm = *reinterpret_cast<FixSmem<N>*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int p0 = (blockIdx.x % p.pblocks) * kPB;
+  const int64_t ci = (blockIdx.x / p.pblocks) % p.cps;  // chunk within the segment
+  const int seg = 1 + static_cast<int>((blockIdx.x / p.pblocks / p.cps) % (p.nseg - 1));
+  const int64_t bh = blockIdx.x / p.pblocks / p.cps / (p.nseg - 1);
+  const int64_t b = bh / p.H, h = bh % p.H;
+  const int64_t L = p.L;
+  const int64_t c = seg * p.cps + ci;
+  if (c * kQ >= L) return;  // the last segment can be shorter (whole CTA leaves together)
+  const float A = -ex2(__ldg(p.A_log + h) * kLog2e);
+  constexpr int kPieces = N * 2 / 16;
+  constexpr int kNW = N / 4;
+  constexpr int kMT = kNW / 16;
+
+  // H_seg for this CTA's [N, 16] slice, element (n, pp) in the accumulator layout of the first pass
+  float hs[kMT][2][4];
+  const float* E = p.seg_state + bh * p.nseg * p.P * N;
+  const float* Dl = p.seg_logdec + bh * p.nseg;
+#pragma unroll
+  for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int n = warp * kNW + mt * 16 + (lane >> 2) + ((r & 2) ? 8 : 0);
+        const int64_t pn = static_cast<int64_t>(p0 + nt * 8 + 2 * (lane & 3) + (r & 1)) * N + n;
+        float v = E[pn];  // H_1 = E_0
+        for (int u = 1; u < seg; ++u) v = fmaf(ex2(Dl[u] * kLog2e), v, E[u * p.P * N + pn]);
+        hs[mt][nt][r] = v;
+        if (seg == p.nseg - 1 && ci == 0 && p.final_state)
+          p.final_state[bh * p.P * N + pn] = fmaf(ex2(Dl[seg] * kLog2e), v, E[seg * p.P * N + pn]);
+        // bf16 copy as the MMA operand: written below
+      }
+#pragma unroll
+  for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int n = warp * kNW + mt * 16 + (lane >> 2) + hr * 8;
+        const int col = nt * 8 + 2 * (lane & 3);
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(sm.Sb) + p16_off(n, col >> 3) + (col & 7) * 2) =
+            pack_bf16(hs[mt][nt][2 * hr], hs[mt][nt][2 * hr + 1]);
+      }
+
+  const int mi = lane >> 3, r8 = lane & 7;
+  const int64_t t0 = c * kQ;
+#pragma unroll
+  for (int k = tid; k < kQ * kPieces; k += kThreads) {
+    const int row = k / kPieces, piece = k % kPieces;
+    const bool ok = t0 + row < L;
+    cp_async16(reinterpret_cast<char*>(sm.Ct) + bc_off<N>(row, piece), p.C + (ok ? (b * L + t0 + row) * N + piece * 8 : 0),
+               ok);
+  }
+  cp_async_commit();
+  if (tid < kQ) sm.dt[tid] = (t0 + tid < L) ? p.delta[(b * L + t0 + tid) * p.H + h] : 0.0f;
+  // log decay from the segment start to this chunk's start: A times the sum of delta over those steps
+  float acc = 0.0f;
+  for (int64_t t = seg * p.cps * kQ + tid; t < t0; t += kThreads) acc += p.delta[(b * L + t) * p.H + h];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) sm.part[warp] = acc;
+  cp_async_wait_all();
+  __syncthreads();  // C tile, dt, partial sums and the state copy are visible
+  {
+    if (warp == 0) {  // cum_i = off + running sum of delta A through step i
+      float off = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) off += sm.part[w];
+      off *= A;
+      const float v0 = sm.dt[2 * lane] * A, v1 = v0 + sm.dt[2 * lane + 1] * A;
+      float inc = v1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+      }
+      float before = __shfl_up_sync(0xffffffffu, inc, 1);
+      if (lane == 0) before = 0.0f;
+      sm.cum[2 * lane] = off + before + v0;
+      sm.cum[2 * lane + 1] = off + before + v1;
+    }
+    __syncthreads();
+    const uint32_t Cb = smem_u32(sm.Ct), Sbb = smem_u32(sm.Sb);
+    float y2[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) y2[nt][r] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < N / 16; ++kk) {
+      uint32_t a[4], b0, b1, b2, b3;
+      ldsm_x4(Cb + bc_off<N>(warp * 16 + (mi & 1) * 8 + r8, kk * 2 + (mi >> 1)), a[0], a[1], a[2], a[3]);
+      ldsm_x4_t(Sbb + p16_off(kk * 16 + (mi & 1) * 8 + r8, mi >> 1), b0, b1, b2, b3);
+      mma_bf16(y2[0], a, b0, b1);
+      mma_bf16(y2[1], a, b2, b3);
+    }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      const int i = warp * 16 + (lane >> 2) + hr * 8;
+      const int64_t t = t0 + i;
+      if (t < L) {
+        const float e = ex2(sm.cum[i] * kLog2e);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          uint32_t* yp = reinterpret_cast<uint32_t*>(p.y + ((b * L + t) * p.H + h) * p.P + p0 + nt * 8 + 2 * (lane & 3));
+          const uint32_t old = *yp;
+          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&old);
+          *yp = pack_bf16(fmaf(e, y2[nt][2 * hr], __low2float(v)), fmaf(e, y2[nt][2 * hr + 1], __high2float(v)));
+        }
+      }
+    }
+  }
+}
+
+// Opt a kernel in to its dynamic shared memory once per device. Keyed by the kernel itself (every kernel
+// here has the same type, so a type parameter would share one flag between them).
+template <auto Kern>
+cudaError_t smem_attr_once(size_t smem) {
+  static bool attr_set[64] = {false};
+  auto kern = Kern;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!attr_set[dev & 63]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev & 63] = true;
+  }
+  return cudaSuccess;
 }
 
 template <int N, bool ZOH>
 cudaError_t launch_ssd_n(const SsdParams& sp, cudaStream_t s) {
-  const size_t smem = sizeof(SsdSmem<N>);
   auto kern = ssd_fwd_kernel<N, ZOH>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = smem_attr_once<ssd_fwd_kernel<N, ZOH>>(sizeof(SsdSmem<N>));
   if (e != cudaSuccess) return e;
-  const int64_t blocks = sp.batch * sp.H * sp.pblocks;
-  kern<<<static_cast<unsigned>(blocks), kThreads, smem, s>>>(sp);
+  const int64_t blocks = sp.batch * sp.H * sp.pblocks * sp.nseg;
+  kern<<<static_cast<unsigned>(blocks), kThreads, sizeof(SsdSmem<N>), s>>>(sp);
+  if ((e = cudaGetLastError()) != cudaSuccess || sp.nseg == 1) return e;
+  auto fix = ssd_fixup_kernel<N>;
+  if ((e = smem_attr_once<ssd_fixup_kernel<N>>(sizeof(FixSmem<N>))) != cudaSuccess) return e;
+  const int64_t fblocks = sp.batch * sp.H * sp.pblocks * (sp.nseg - 1) * sp.cps;
+  fix<<<static_cast<unsigned>(fblocks), kThreads, sizeof(FixSmem<N>), s>>>(sp);
   return cudaGetLastError();
+}
+
+// Segments per sequence: only when one CTA per sequence would leave SMs idle (fewer CTAs than SMs), then
+// enough for one CTA per SM, segments of at least 4 chunks, at most 16. With 192 CTAs on 148 SMs, two
+// segments per sequence measured slower (111 us against 84 us): the per-chunk work of the resident CTAs
+// already shares each SM, so splitting only pays where SMs would otherwise sit idle.
+void ssd_segments(int64_t batch, int64_t L, int64_t H, int64_t P, int* nseg, int64_t* cps) {
+  const int64_t nchunks = (L + kQ - 1) / kQ;
+  const int64_t ctas = batch * H * (P / kPB);
+  const int64_t sms = sm_count();
+  int64_t s = (ctas > 0 && ctas < sms) ? (sms + ctas - 1) / ctas : 1;
+  const int64_t by_len = nchunks / 4;
+  if (s > by_len) s = by_len;
+  if (s > 16) s = 16;
+  if (s < 1) s = 1;
+  const int64_t c = (nchunks + s - 1) / s;  // chunks per segment; no segment is left empty
+  *cps = c > 0 ? c : 1;
+  *nseg = static_cast<int>(c > 0 ? (nchunks + c - 1) / c : 1);
 }
 
 }  // namespace
 
 bool ssd_shape_ok(int64_t P, int64_t N) { return (N == 64 || N == 128) && P > 0 && P % kPB == 0; }
+
+size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N) {
+  int nseg = 1;
+  int64_t cps = 1;
+  ssd_segments(batch, L, H, P, &nseg, &cps);
+  if (nseg <= 1) return 0;
+  return static_cast<size_t>(batch * H * nseg) * static_cast<size_t>(P * N + 1) * sizeof(float);
+}
 
 cudaError_t launch_ssd(const SsdArgs& a) {
   SsdParams sp;
@@ -394,6 +591,22 @@ cudaError_t launch_ssd(const SsdArgs& a) {
   sp.final_state = a.final_state;
   sp.batch = a.batch; sp.L = a.L; sp.H = a.H; sp.P = a.P;
   sp.pblocks = static_cast<int>(a.P / kPB);
+  sp.nseg = 1;
+  sp.cps = (a.L + kQ - 1) / kQ;
+  sp.seg_state = nullptr;
+  sp.seg_logdec = nullptr;
+  const size_t need = ssd_workspace_bytes(a.batch, a.L, a.H, a.P, a.N);
+  if (need > 0 && a.workspace && a.workspace_bytes >= need) {  // without it, one CTA walks each sequence
+    ssd_segments(a.batch, a.L, a.H, a.P, &sp.nseg, &sp.cps);
+    if (a.batch * a.H * sp.pblocks * sp.nseg * sp.cps > INT32_MAX) {  // grid too large: one CTA per sequence
+      sp.nseg = 1;
+      sp.cps = (a.L + kQ - 1) / kQ;
+    }
+    if (sp.nseg > 1) {
+      sp.seg_state = static_cast<float*>(a.workspace);
+      sp.seg_logdec = sp.seg_state + a.batch * a.H * sp.nseg * a.P * a.N;
+    }
+  }
   if (a.N == 64) return a.disc == 1 ? launch_ssd_n<64, true>(sp, a.stream) : launch_ssd_n<64, false>(sp, a.stream);
   return a.disc == 1 ? launch_ssd_n<128, true>(sp, a.stream) : launch_ssd_n<128, false>(sp, a.stream);
 }

@@ -15,7 +15,7 @@ def _bf16(torch, a_bits, shape):
     return torch.from_numpy(a_bits.view(np.int16).copy()).view(torch.bfloat16).reshape(shape).cuda()
 
 
-def _run(orc, batch, L, H, P, N, disc, with_h0, seed):
+def _run(orc, batch, L, H, P, N, disc, with_h0, seed, workspace="auto"):
     import torch
     import selective_state_space_124_b300 as lib
     inp = ssm_inputs.make_ssd_inputs(batch, L, H, P, N, seed=seed)
@@ -25,7 +25,8 @@ def _run(orc, batch, L, H, P, N, disc, with_h0, seed):
     C = _bf16(torch, inp["C_bits"], (batch, L, N))
     dt = torch.from_numpy(inp["delta"]).cuda()
     A = torch.from_numpy(inp["A_log"]).cuda()
-    y, fs = lib.ssm_ssd_fwd(x, dt, A, B, C, disc=disc, h0=None if h0 is None else torch.from_numpy(h0).cuda())
+    y, fs = lib.ssm_ssd_fwd(x, dt, A, B, C, disc=disc, h0=None if h0 is None else torch.from_numpy(h0).cuda(),
+                            workspace=workspace)
     lib.check_device()
     yr, sr = orc.ssd_fwd(inp["x"], inp["delta"], inp["A_log"], inp["B"], inp["C"], disc=disc, h0=h0)
     return y.float().cpu().numpy(), fs.cpu().numpy(), yr, sr
@@ -44,6 +45,24 @@ def test_ssd_parity(orc, shape, disc, with_h0):
     ey, es = rel_err(y, yr), rel_err(fs, sr)
     assert ey <= TOL["bf16"], f"y rel err {ey:.3g}"
     assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
+
+
+# long enough sequences for several segments per sequence (each scanned by its own CTAs, then fixed up)
+SEG_SHAPES = [(1, 1000, 2, 64, 128), (1, 700, 1, 16, 64), (2, 2048, 3, 32, 128)]
+
+
+@pytest.mark.parametrize("shape", SEG_SHAPES, ids=[f"b{s[0]}_L{s[1]}_H{s[2]}_P{s[3]}_N{s[4]}" for s in SEG_SHAPES])
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("with_h0", [False, True], ids=["zero_state", "h0"])
+def test_ssd_segments_match_one_cta_per_sequence(orc, shape, disc, with_h0):
+    """With and without the segment workspace: both against the oracle, and the segmented run really splits."""
+    import selective_state_space_124_b300 as lib
+    assert lib.ssd_workspace_size(shape[0], shape[1], shape[2], shape[3], shape[4]) > 0
+    for ws in ("auto", None):
+        y, fs, yr, sr = _run(orc, *shape, disc, with_h0, seed=sum(shape) + 1, workspace=ws)
+        ey, es = rel_err(y, yr), rel_err(fs, sr)
+        assert ey <= TOL["bf16"], f"workspace {ws}: y rel err {ey:.3g}"
+        assert es <= TOL["bf16"], f"workspace {ws}: final state rel err {es:.3g}"
 
 
 def test_ssd_empty_sequence():
