@@ -116,6 +116,37 @@ def test_bwd_argument_errors(lib):
     assert bwd(lib, batch=1 << 40, L=1 << 20, D=1 << 20) == _ffi.SSM_ERR_INVALID_ARG
 
 
+def ssd(lib, *, x=FAKE, y=FAKE + (6 << 30), ws=None, ws_bytes=0, batch=2, L=256, H=4, P=64, N=128, dtype=1, disc=0,
+        final=FAKE + (7 << 30)):
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+    return lib.ssm_ssd_fwd(v(x), v(FAKE + (1 << 30)), v(FAKE + (2 << 30)), v(FAKE + (3 << 30)), v(FAKE + (4 << 30)),
+                           None, v(y), v(final), v(ws), ws_bytes, batch, L, H, P, N, dtype, disc, None)
+
+
+def test_ssd_argument_errors(lib):
+    assert ssd(lib, dtype=0) == _ffi.SSM_ERR_UNSUPPORTED              # fp32 activations: bf16 only
+    assert b"bf16" in lib.ssm_last_error()
+    assert ssd(lib, N=96) == _ffi.SSM_ERR_UNSUPPORTED                 # N must be 64 or 128
+    assert ssd(lib, P=24) == _ffi.SSM_ERR_UNSUPPORTED                 # P a multiple of 16
+    assert ssd(lib, x=FAKE + 8) == _ffi.SSM_ERR_UNSUPPORTED           # 16-byte alignment
+    assert ssd(lib, L=-1) == _ffi.SSM_ERR_INVALID_ARG
+    assert ssd(lib, disc=3) == _ffi.SSM_ERR_INVALID_ARG
+    assert ssd(lib, x=None) == _ffi.SSM_ERR_INVALID_ARG
+    assert ssd(lib, y=FAKE + 64) == _ffi.SSM_ERR_INVALID_ARG          # y overlaps x
+    assert ssd(lib, final=FAKE + (6 << 30) + 16) == _ffi.SSM_ERR_INVALID_ARG      # final state overlaps y
+    assert ssd(lib, ws=FAKE + (1 << 30), ws_bytes=64) == _ffi.SSM_ERR_INVALID_ARG  # workspace overlaps delta
+    assert ssd(lib, batch=0) == _ffi.SSM_OK                           # nothing to do, no GPU touched
+
+
+def test_ssd_workspace_size(lib):
+    # segments only where one CTA per sequence (batch x heads x P / 16) leaves SMs idle, each of >= 4 chunks
+    assert lib.ssm_ssd_fwd_workspace_size(8, 4096, 24, 64, 128) == 0    # 768 CTAs: no split
+    assert lib.ssm_ssd_fwd_workspace_size(1, 100, 2, 64, 128) == 0      # 2 chunks: too short to split
+    nbytes = lib.ssm_ssd_fwd_workspace_size(1, 1000, 2, 64, 128)        # 8 CTAs, 16 chunks -> 4 segments
+    assert nbytes == 1 * 2 * 4 * (64 * 128 + 1) * 4
+    assert lib.ssm_ssd_fwd_workspace_size(1, 1000, 2, 64, 96) == 0      # unsupported N
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         _ffi.load(str(tmp_path / "libssm_scan.so"))
