@@ -19,6 +19,11 @@
 // Products use the warp-level bf16 tensor-core MMA (m16n8k16, fp32 accumulate); operands come from
 // shared memory through ldmatrix. The next chunk's x, B, C tiles stream in with cp.async while the
 // current one is computed.
+//
+// Segments (optional caller workspace, used when one CTA per sequence would leave SMs idle): each sequence
+// is cut into runs of chunks that separate CTAs scan from a zero state, recording each run's end state and
+// total log decay; ssd_fixup_kernel then carries the true state into every run and adds its contribution
+// e^{cum_i} C_i . H to the outputs, one CTA per chunk.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
