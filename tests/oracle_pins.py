@@ -499,6 +499,32 @@ def pin_bwd_split(orc):
         _close(g1["dh0"], g["dh0"], 1e-12, f"split dh0 ({disc})")
 
 
+def pin_bwd_channel_subset(orc):
+    """The per-channel outputs of a channel subset equal the full evaluation's (dx, ddelta, dh0), and the
+    per-channel contributions add up to the full dA_log, dB and dC."""
+    rng = np.random.default_rng(24)
+    batch, L, D, N = 2, 9, 3, 4
+    x, dt, A_log, B, C, dy, h0, dfinal = _bwd_problem(rng, batch, L, D, N, 0.3, 3.0, 0.05, 0.7)
+    g = orc.scan_bwd(x, dt, A_log, B, C, dy, disc="zoh", h0=h0, dfinal=dfinal, f64=True)
+    chans = [4, 1, 5, 0, 2, 3]
+    gs = orc.scan_bwd(x, dt, A_log, B, C, dy, disc="zoh", h0=h0.reshape(batch * D, N)[chans],
+                      dfinal=dfinal.reshape(batch * D, N)[chans], channels=chans, f64=True)
+    dA = np.zeros((D, N))
+    dB = np.zeros((batch, L, N))
+    dC = np.zeros((batch, L, N))
+    for i, c in enumerate(chans):
+        b, d = divmod(c, D)
+        _close(gs["dx"][i], g["dx"][b, :, d], 1e-14, "subset dx")
+        _close(gs["ddelta"][i], g["ddelta"][b, :, d], 1e-14, "subset ddelta")
+        _close(gs["dh0"][i], g["dh0"][b, d], 1e-14, "subset dh0")
+        dA[d] += gs["dA_log"][i]
+        dB[b] += gs["dB"][i]
+        dC[b] += gs["dC"][i]
+    _close(dA, g["dA_log"], 1e-13, "subset dA_log sum")
+    _close(dB, g["dB"], 1e-13, "subset dB sum")
+    _close(dC, g["dC"], 1e-13, "subset dC sum")
+
+
 # --- Mamba-2 SSD layer (scalar A per head) -----------------------------------------------------------------
 
 def _ssd_problem(rng, batch, L, H, P, N):
@@ -559,6 +585,7 @@ ALL_PINS = [
     pin_lti_zoh_example, pin_convolution_view, pin_selective_zoh_example, pin_combine_tree,
     pin_small_delta_limit, pin_unit_input_two_step, pin_delta_limits, pin_brute_force_1ss,
     pin_split_and_step, pin_softplus_inside_scan, pin_feedthrough_and_gate, pin_bwd_finite_differences,
-    pin_bwd_convolution_adjoint, pin_bwd_one_step, pin_bwd_split, pin_ssd_is_the_scan_with_shared_decay,
+    pin_bwd_convolution_adjoint, pin_bwd_one_step, pin_bwd_split, pin_bwd_channel_subset,
+    pin_ssd_is_the_scan_with_shared_decay,
     pin_ssd_chunked_duality, pin_ssd_running_example,
 ]

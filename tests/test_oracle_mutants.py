@@ -63,6 +63,8 @@ MUTANTS = {
                            "yv += ld(B, (b * L + t) * N + n, is_f64) * S[p * N + n];"),
     "ssd_h0_ignored": ("for (int64_t i = 0; i < P * N; ++i) S[i] = h0 ? h0[k * P * N + i] : 0.0;",
                        "for (int64_t i = 0; i < P * N; ++i) S[i] = 0.0;"),
+    "bwd_dy_lagged": ("double dyt = ld(dy, (b * L + t) * D + d, is_f64);",
+                      "double dyt = ld(dy, (b * L + (t > 0 ? t - 1 : 0)) * D + d, is_f64);"),
     "channel_index_swapped": ("int64_t b = flat / D, d = flat % D;\n        double h[",
                               "int64_t d = flat / D, b = flat % D;\n        double h["),
 }
