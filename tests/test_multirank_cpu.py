@@ -66,3 +66,24 @@ def test_bench_size_overrides_parse():
     import bench
     a = bench.parse_args(["--workload", "long", "--set", "L=16384", "--set", "batch=2", "--no-extra"])
     assert a.workload == "long" and a.set == ["L=16384", "batch=2"] and a.no_extra
+
+
+def test_compulsory_byte_and_flop_counts():
+    """The roofline numerators, counted by hand for small layers (fp32 and bf16 prefill, decode step,
+    backward, SSD)."""
+    import bench
+    f32 = dict(batch=2, L=3, D=5, N=4, dtype="f32")
+    # x, delta, y: 3 * 30 * 4; B, C: 2 * 6 * 4 * 4; A_log 20 * 4; final state 40 * 4
+    assert bench.fwd_bytes(f32) == 360 + 192 + 80 + 160
+    bf = dict(f32, dtype="bf16")
+    assert bench.fwd_bytes(bf) == 180 + 96 + 80 + 160
+    # x, delta, dy, dx, ddelta: 5 * 30 * 4; B, C: 2 * 24 * 4; dB, dC: 2 * 24 * 4; A_log, dA_log; dh0
+    assert bench.bwd_bytes(f32) == 600 + 192 + 192 + 160 + 160
+    step = dict(batch=2, D=5, N=4, dtype="f32")
+    # state read + write 2 * 40 * 4; x_t, delta_t, y_t 3 * 10 * 4; B_t, C_t 2 * 8 * 4; A_log 20 * 4
+    assert bench.step_bytes(step) == 320 + 120 + 64 + 80
+    ssd = dict(batch=1, L=64, H=2, P=16, N=64)
+    # x, y: 2 * 2048 * 2; B, C: 2 * 4096 * 2; delta 128 * 4; A_log 2 * 4; final state 2048 * 4
+    assert bench.ssd_bytes(ssd) == 8192 + 16384 + 512 + 8 + 8192
+    # one chunk per head: 2 Q^2 N + 2 Q^2 P + 4 Q N P with Q = 64
+    assert bench.ssd_flops(ssd) == 2 * (2 * 64 * 64 * 64 + 2 * 64 * 64 * 16 + 4 * 64 * 64 * 16)
