@@ -15,8 +15,9 @@
  *   final_state[b, d, :] = h after the last step.
  *
  * The first-order (Euler) input term keeps the exact Abar, as the pages' scalar recurrence and the
- * aiwiki reference loop do ("State Space Models & Mamba" chapter; aiwiki entry: delta*B "is what Mamba
- * itself uses"). delta is taken as given (already made positive upstream; no softplus inside).
+ * aiwiki reference loop do ("State Space Models & Mamba" chapter; the aiwiki entry names delta*B as the
+ * form Mamba uses in practice). delta is taken as given (already made positive upstream); the _ex entry
+ * points can apply softplus(delta + bias) themselves.
  *
  * Conventions shared by every entry point:
  *  - Every pointer is DEVICE memory of the current CUDA device, owned by the caller. No call allocates or
@@ -27,7 +28,8 @@
  *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy default
  *    stream) and runs asynchronously; the return code covers argument checks and launch errors.
  *    ssm_check_device() synchronises the stream and reports errors raised while kernels ran.
- *  - N (state size) must be in [1, 16]; larger N returns SSM_ERR_UNSUPPORTED.
+ *  - For the diagonal scan, N (state size) must be in [1, 16]; larger N returns SSM_ERR_UNSUPPORTED. The
+ *    SSD layer has its own sizes (see ssm_ssd_fwd).
  *  - Outputs may not overlap inputs (checked on the pointer ranges: SSM_ERR_INVALID_ARG).
  *  - Any status other than SSM_OK leaves a one-line reason in ssm_last_error() (per thread).
  *  - Results are deterministic for a given shape, dtype and device (no atomics on the data path), except

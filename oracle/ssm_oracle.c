@@ -12,7 +12,7 @@
  *                                                   the same exact Abar is kept in the first-order form
  *                                                   ("State Space Models & Mamba" chapter, scalar
  *                                                   selective recurrence and its code)
- *   bbar*x = Euler: delta * B[b,t,n] * x[b,t,d]    aiwiki entry (dt * B, "what Mamba itself uses");
+ *   bbar*x = Euler: delta * B[b,t,n] * x[b,t,d]    aiwiki entry (dt * B, named there as the form Mamba uses);
  *                                                   chapter's Euler-simplified Bbar = delta * B
  *            ZOH:   expm1(delta*A[n]) / A[n] * B[b,t,n] * x[b,t,d]
  *                                                   "Understanding Mamba" s2.2 Eq. (2) second half,
