@@ -1,9 +1,12 @@
 #!/usr/bin/env python
 """Benchmark of the selective scan's hot path on B300; prints one JSON line (rank 0).
 
-One step = the whole path on one batch of synthetic input: ssm_scan_fwd over the Mamba-130M-shaped
-layer (batch 2, L 2048, D 1536, N 16, fp32, Euler), then one ssm_scan_step continuing from its final
-state (the prefill -> decode hand-off). Units per step: batch * (L + 1) * D scan elements.
+One step = the whole path on one batch of synthetic input: ssm_scan_fwd over the long-sequence
+workload (batch 1, L 131072, D 1536, N 16, fp32, exact ZOH; 2.43 GB of compulsory traffic, far larger
+than L2), then one ssm_scan_step continuing from its final state (the prefill -> decode hand-off).
+Units per step: batch * (L + 1) * D scan elements. The other prefill workloads (the Mamba-130M and
+Mamba-1.4B layers), the fused layer, the backward pass, the SSD layer and the decode workload are timed
+after it and reported under "workloads".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
@@ -45,15 +48,20 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mamba130m",
+    ap.add_argument("--workload", default="long",
                     choices=sorted(k for k in ssm_inputs.WORKLOADS if k != "decode"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    ap.add_argument("--cpu-seconds", type=float, default=None,
+                    help="CPU oracle seconds per sample (default: 5 for the GPU arm's baseline, "
+                         "120 / (steps + warmup) for --impl reference)")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
                     help="override a size of the workload (batch, L or D), e.g. for a small profiling case")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads (reported under 'workloads')")
+    ap.add_argument("--profile", action="store_true",
+                    help="a lean run for profilers: no L2-flush buffers, no other workloads, no end-to-end leg, "
+                         "no CPU baseline (its timings are not benchmark values)")
     ap.add_argument("--extra", default="all", metavar="KIND[,KIND]",
                     help="which other workloads to time: all, or any of prefill, fused, bwd, ssd, decode")
     return ap.parse_args(argv)
@@ -488,6 +496,20 @@ def job_value(units_per_step: int, steps: int, world: int, seconds: float) -> fl
     return world * units_per_step * steps / seconds
 
 
+def oracle_threads() -> int:
+    """Threads the CPU oracle runs on: every host core this process may use."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def pin_oracle_threads() -> None:
+    """Fix the oracle's OpenMP thread count before its library (and so libgomp) is loaded, so that both
+    bench arms time it on the same number of threads."""
+    os.environ["OMP_NUM_THREADS"] = str(oracle_threads())
+
+
 def oracle_sample(inp, cfg, budget_s):
     """Pick a channel subset whose whole sequences take about budget_s seconds in the oracle."""
     import oracle
@@ -514,12 +536,34 @@ def cpu_oracle_rate(inp, cfg, chans):
     return n * L / dt, orc.num_threads(), f"{n} of {total} channels, full L = {L} each ({n * L} elems)"
 
 
+def workload_config(args, world):
+    """Size overrides and the JSON `config` of a run; both arms report the same config."""
+    overrides = {}
+    for kv in args.set:
+        k, v = kv.split("=", 1)
+        if k not in ("batch", "L", "D"):
+            raise SystemExit(f"--set: unknown size {k!r} (batch, L or D)")
+        overrides[k] = int(v)
+    cfg = dict(ssm_inputs.WORKLOADS[args.workload], **overrides)
+    es = 2 if cfg["dtype"] == "bf16" else 4
+    in_bytes = cfg["batch"] * cfg["L"] * (2 * cfg["D"] + 2 * cfg["N"]) * es
+    config = {"workload": describe(args.workload, cfg),
+              "l2": f"L2 flushed (512 MiB write) before every step; prefill inputs {in_bytes / 1e9:.3g} GB "
+                    f"({'larger' if in_bytes > 126e6 else 'smaller'} than the 126 MB L2)",
+              "parallelism": f"weak x{world}: one independent batch per GPU (seed = rank), no collective"}
+    return overrides, cfg, config
+
+
 def run_reference(args, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores, one bounded sample per step."""
     if rank != 0:
         return
-    cfg = dict(ssm_inputs.WORKLOADS[args.workload])
-    inp = ssm_inputs.workload_inputs(args.workload)
-    chans = oracle_sample(inp, cfg, max(0.02, 120.0 / max(1, args.steps + args.warmup)))
+    pin_oracle_threads()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    overrides, cfg, config = workload_config(args, world)
+    inp = ssm_inputs.workload_inputs(args.workload, **overrides)
+    budget = args.cpu_seconds if args.cpu_seconds is not None else 120.0 / max(1, args.steps + args.warmup)
+    chans = oracle_sample(inp, cfg, max(0.02, budget))
     rates, cores, sample = [], None, None
     for i in range(args.warmup + args.steps):
         r, cores, sample = cpu_oracle_rate(inp, cfg, chans)
@@ -531,12 +575,34 @@ def run_reference(args, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "elems/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": units / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": describe(args.workload, cfg), "l2": "n/a (host)"},
+        "data": "synthetic", "config": config,
         "cpu_baseline": {"value": value, "unit": "elems/s", "cores": cores, "kind": "oracle",
                          "sample": "each step: " + sample},
         "e2e": {"value": value, "unit": "elems/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }), flush=True)
+
+
+def cpu_baseline_subprocess(args):
+    """The oracle timed in a fresh process (no torch, no CUDA context, OpenMP pinned to the host cores),
+    exactly as the reference arm times it: 1 untimed and 2 timed samples of the same workload."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", args.workload,
+           "--steps", "2", "--warmup", "1", "--cpu-seconds", str(args.cpu_seconds or 5.0)]
+    for kv in args.set:
+        cmd += ["--set", kv]
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "LOCAL_WORLD_SIZE", "GROUP_RANK", "ROLE_RANK",
+                        "TORCHELASTIC_RUN_ID", "MASTER_ADDR", "MASTER_PORT")}
+    env["OMP_NUM_THREADS"] = str(oracle_threads())
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900, check=True).stdout
+        rec = json.loads(out.strip().splitlines()[-1])["cpu_baseline"]
+    except (subprocess.SubprocessError, ValueError, KeyError, IndexError) as e:
+        return {"value": None, "unit": "elems/s", "cores": None, "kind": "oracle",
+                "sample": f"unavailable: {type(e).__name__}: {str(e)[:200]}"}
+    rec["sample"] = rec["sample"].replace("each step: ", "median of 2 timed samples, each ")
+    rec["process"] = "separate process, OMP_NUM_THREADS = host cores (as the reference arm)"
+    return rec
 
 
 def main(argv=None):
@@ -554,13 +620,7 @@ def main(argv=None):
     if world > 1:
         dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
 
-    overrides = {}
-    for kv in args.set:
-        k, v = kv.split("=", 1)
-        if k not in ("batch", "L", "D"):
-            raise SystemExit(f"--set: unknown size {k!r} (batch, L or D)")
-        overrides[k] = int(v)
-    cfg = dict(ssm_inputs.WORKLOADS[args.workload], **overrides)
+    overrides, cfg, config = workload_config(args, world)
     inp = ssm_inputs.workload_inputs(args.workload, seed=rank_seed(rank), **overrides)
     tok = ssm_inputs.token_inputs(cfg["batch"], cfg["D"], cfg["N"], seed=1000 + rank_seed(rank),
                                   mu=cfg["mu"], sigma=cfg["sigma"])
@@ -581,7 +641,9 @@ def main(argv=None):
     y = torch.empty((b, L, D), dtype=tdt, device="cuda")
     state = torch.empty((b, D, N), dtype=torch.float32, device="cuda")
     y_t = torch.empty((b, D), dtype=tdt, device="cuda")
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    if args.profile:
+        args.no_extra = args.no_e2e = args.no_cpu_baseline = True
+    flush = torch.empty(FLUSH_BYTES // 4 if not args.profile else 256, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
     # The timed loop calls the C ABI on precomputed device addresses: launching costs a few microseconds of
@@ -611,7 +673,7 @@ def main(argv=None):
         dist.barrier()
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
-    head = torch.empty(4 * FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    head = torch.empty(4 * FLUSH_BYTES // 4 if not args.profile else 256, dtype=torch.float32, device="cuda")
     with sampler:
         wall0 = time.perf_counter()
         head.zero_()  # a long first write: the host enqueues ahead of the device from the start
@@ -676,8 +738,7 @@ def main(argv=None):
         "metric": METRIC, "value": value, "unit": "elems/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": total_s / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg["dtype"], "data": "synthetic",
-        "config": {"workload": describe(args.workload, cfg), "l2": "flushed (512 MiB write) before every step",
-                   "parallelism": f"weak x{world}: one independent batch per GPU (seed = rank), no collective"},
+        "config": config,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic("scan_fwd", args.workload),
                      "peak_kind": peak_kind, "kernel": "ssm_scan_fwd",
@@ -693,21 +754,20 @@ def main(argv=None):
         kinds = set(args.extra.split(",")) if args.extra != "all" else {"prefill", "fused", "bwd", "ssd", "decode"}
         extra = {}
         if "prefill" in kinds:
-            for name in ("long", "mamba1p4b"):
+            for name in ("long", "mamba130m", "mamba1p4b"):
                 if name != args.workload:
                     extra[name] = measure_prefill(name, 10, flush, peak)
-        if "fused" in kinds:
-            extra[args.workload + "_fused"] = measure_prefill(args.workload, 10, flush, peak, fused=True)
+        if "fused" in kinds:  # the layer pieces and the backward pass on the Mamba-130M-shaped layer
+            extra["mamba130m_fused"] = measure_prefill("mamba130m", 10, flush, peak, fused=True)
         if "bwd" in kinds:
-            extra[args.workload + "_bwd"] = measure_backward(args.workload, 10, flush, peak)
+            extra["mamba130m_bwd"] = measure_backward("mamba130m", 10, flush, peak)
         if "ssd" in kinds:
             extra["mamba2_130m_ssd"] = measure_ssd("mamba2_130m", 10, flush, peak)
         if "decode" in kinds:
             extra["decode"] = measure_decode(1000, flush, peak)
         line["workloads"] = extra
     if not args.no_cpu_baseline:
-        r, cores, sample = cpu_oracle_rate(inp, cfg, oracle_sample(inp, cfg, args.cpu_seconds))
-        line["cpu_baseline"] = {"value": r, "unit": "elems/s", "cores": cores, "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = cpu_baseline_subprocess(args)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

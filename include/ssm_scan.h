@@ -22,7 +22,11 @@
  * Conventions shared by every entry point:
  *  - Every pointer is DEVICE memory of the current CUDA device, owned by the caller. No call allocates or
  *    frees memory, and none keeps a pointer after it returns. The one exception: ssm_scan_bwd_noalloc
- *    uses a fixed 64 MiB scratch array, which every device that loads the library reserves at load time.
+ *    uses a fixed 64 MiB scratch array compiled into the backward pass's device code. The CUDA runtime
+ *    loads that code onto a device the first time a backward entry point (ssm_scan_bwd or
+ *    ssm_scan_bwd_noalloc) runs there (module loading is lazy by default; with
+ *    CUDA_MODULE_LOADING=EAGER it happens when the process's context on the device is created), and the
+ *    64 MiB stay committed on that device until the process exits, for ssm_scan_bwd callers too.
  *  - Layouts are dense row-major in the shapes given. "dtype" arrays hold fp32 (SSM_DTYPE_F32) or
  *    bf16 (SSM_DTYPE_BF16) elements; A_log, states, h0 and final_state are always fp32.
  *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy default
@@ -51,7 +55,8 @@ typedef enum {
     SSM_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum, overlapping in/out ranges */
     SSM_ERR_UNSUPPORTED = 2,  /* valid but not implemented (N > 16) */
     SSM_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
-    SSM_ERR_TIMEOUT = 4       /* a kernel gave up a bounded wait (reported by ssm_check_device) */
+    SSM_ERR_TIMEOUT = 4       /* a kernel gave up a bounded wait (reported by ssm_check_device; see
+                                 ssm_set_wait_limit_ns) */
 } ssm_status;
 
 typedef enum { SSM_DISC_EULER = 0, SSM_DISC_ZOH = 1 } ssm_disc;
@@ -160,12 +165,15 @@ size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t L, int64_t D, int64_t 
  * stall or fail at the worst moment). It has no counterpart in the pages: it is a packaging choice of this
  * library, not part of the method.
  *
- * The chunk-end states live in a scratch array inside the library itself (64 MiB, reserved on every
- * device that loads the library until the process exits). Sizes whose ssm_scan_bwd_workspace_size()
- * exceeds 64 MiB return SSM_ERR_INVALID_ARG with a message saying so (use ssm_scan_bwd with a workspace
- * then). The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. The first
- * call on a device looks up the array's device address on that device; make that first call before any
- * stream capture. All calls on a device share the one array, so two calls whose kernels may run at the
+ * The chunk-end states live in a scratch array inside the library itself: 64 MiB of device memory,
+ * committed on a device when the backward pass's device code is first loaded there (the first call of
+ * ssm_scan_bwd or ssm_scan_bwd_noalloc on that device, unless CUDA_MODULE_LOADING=EAGER loads it with the
+ * context) and held until the process exits. The call itself allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine; but that first load does take the 64 MiB from the device, so a
+ * caller that may not allocate while serving should make one call at start-up, before serving and before
+ * any stream capture (a call with batch, L and D all 0 and null data pointers is enough: it loads the code
+ * and looks up the array's address on the current device, and computes nothing). Sizes whose ssm_scan_bwd_workspace_size() exceeds
+ * 64 MiB return SSM_ERR_INVALID_ARG with a message saying so (use ssm_scan_bwd with a workspace then). All calls on a device share the one array, so two calls whose kernels may run at the
  * same time on that device (other streams, other host threads) race on it and give wrong gradients:
  * serialise them. The array needs no clearing between calls (each call writes every entry it reads).
  * Arguments, outputs and errors otherwise as for ssm_scan_bwd.
@@ -211,6 +219,19 @@ size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t P
 
 /* Synchronise `stream` and report any error raised while this library's kernels ran on it. */
 ssm_status ssm_check_device(void *stream);
+
+/*
+ * Longest time, in nanoseconds, that a warp of the prefill kernel for N = 16 (the TMA-staged one) waits
+ * for one staged tile of its inputs before giving up. The default is 2,000,000,000 (2 s); a healthy tile
+ * arrives within microseconds. A warp that gives up stops its share of the scan and sets the library's
+ * device status word, so that the next ssm_check_device() returns SSM_ERR_TIMEOUT; that launch's y and
+ * final_state are then incomplete. A warp waits for the copies it still has in flight before it exits
+ * (that wait keeps the fixed 2 s bound), so a launch that gives up leaves no copy writing into shared
+ * memory and the device stays usable. The setting is process-wide, applies to launches made after the
+ * call, and is read when each launch is enqueued. Returns the previous value. No counterpart in the
+ * pages: this is the library's failure-reporting contract.
+ */
+uint64_t ssm_set_wait_limit_ns(uint64_t ns);
 
 /* Static name of a status code. */
 const char *ssm_status_string(ssm_status s);

@@ -21,7 +21,8 @@ from . import _ffi
 from ._ffi import SsmError
 
 __all__ = ["ssm_scan_fwd", "ssm_scan_step", "ssm_scan_bwd", "ssm_scan_fwd_ptr", "ssm_scan_step_ptr",
-           "bwd_workspace_size", "ssm_ssd_fwd", "ssd_workspace_size", "check_device", "SsmError", "version"]
+           "bwd_workspace_size", "ssm_ssd_fwd", "ssd_workspace_size", "check_device", "set_wait_limit_ns", "SsmError",
+           "version"]
 
 
 def _torch():
@@ -242,6 +243,13 @@ def ssm_ssd_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, want_fin
                                  ctypes_void(s.cuda_stream))
     _ffi.check("ssm_ssd_fwd", st)
     return y, fs
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Bound, in nanoseconds, on one wait of the TMA prefill kernel for a staged tile (default 2 s); a wait
+    that runs out makes the next check_device() raise SsmError with status SSM_ERR_TIMEOUT. Returns the
+    previous bound."""
+    return int(_ffi.load().ssm_set_wait_limit_ns(int(ns)))
 
 
 def check_device(stream=None) -> None:

@@ -32,6 +32,7 @@ SIGNATURES = {
                            _i32, _i32, _vp]),
     "ssm_ssd_fwd_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i64, _i64]),
     "ssm_check_device": (_i32, [_vp]),
+    "ssm_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
     "ssm_status_string": (ctypes.c_char_p, [_i32]),
     "ssm_last_error": (ctypes.c_char_p, []),
     "ssm_version": (_i32, []),

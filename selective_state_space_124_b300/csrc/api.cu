@@ -6,10 +6,13 @@
 #include "../../include/ssm_scan.h"
 #include "launch.h"
 
+#include <atomic>
+
 namespace ssm {
 
 namespace {
 thread_local char g_last_error[256] = "";
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
 
 ssm_status fail(ssm_status s, const char* fmt, ...) {
   va_list ap;
@@ -43,6 +46,8 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) {
   return true;
 }
 }  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 int sm_count() {
   static int cached[64] = {0};
@@ -277,6 +282,8 @@ ssm_status ssm_check_device(void* stream) {
   if (st != 0) return fail(SSM_ERR_TIMEOUT, "ssm_check_device: a kernel gave up a bounded wait");
   return SSM_OK;
 }
+
+uint64_t ssm_set_wait_limit_ns(uint64_t ns) { return g_wait_limit_ns.exchange(ns); }
 
 const char* ssm_status_string(ssm_status s) {
   switch (s) {

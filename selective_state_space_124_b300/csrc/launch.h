@@ -82,6 +82,8 @@ struct SsdArgs {
 };
 
 int sm_count();  // multiprocessors of the current device (cached per device)
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // default bound on one consumer wait of a kernel (2 s)
+uint64_t wait_limit_ns();                           // the current bound (ssm_set_wait_limit_ns)
 
 cudaError_t launch_fwd_simple(const FwdArgs& a);
 bool tma_path_ok(const FwdArgs& a);       // N == 16, 16-byte aligned rows and pointers, 32-bit row coords

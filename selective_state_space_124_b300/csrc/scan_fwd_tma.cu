@@ -21,8 +21,8 @@
 // delta and [TS x 16] tiles of B and C; a warm-up ring of NSW stages holds the x, delta, B tiles the
 // backward walk reads. Both rings are filled by cp.async.bulk.tensor (TMA) with mbarrier completion;
 // the forward ring is primed when a range starts, so its copies overlap the warm-up. B and C are read
-// as shared-memory broadcasts (bf16 tiles are widened to fp32 once per stage by the warp, and B is
-// pre-scaled by 1/(n+1) for ZOH). y is stored straight to global memory (a warp writes 32 consecutive
+// as shared-memory broadcasts (bf16 tiles are widened to fp32 once per stage by the warp; for the
+// structured ZOH update the warp also divides B by n + 1 there, once per stage). y is stored straight to global memory (a warp writes 32 consecutive
 // channels of one step). Every wait is bounded (%globaltimer): a wait that runs out sets a device
 // status word that ssm_check_device() reports as SSM_ERR_TIMEOUT.
 //
@@ -52,7 +52,7 @@ __device__ int g_device_status = 0;  // nonzero: a bounded wait ran out (read by
 
 namespace {
 
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s bound on any single mbarrier wait
+constexpr unsigned long long kWaitNs = kDefaultWaitNs;  // 2 s: the bound on the drains before a warp exits
 constexpr float kDeadLog2 = -20.0f;                      // log2 of the decay bound that ends a warm-up
 
 template <typename T, int CPL, int TS, int NSF, int TSW, int NSW>
@@ -65,8 +65,8 @@ struct alignas(128) WarpRing {
   T wx[NSW][TSW * CW];  // warm-up ring: x, delta, B tiles of TSW steps
   T wd[NSW][TSW * CW];
   T wB[NSW][TSW * 16];
-  static constexpr int kConvRows = sizeof(T) == 2 ? TS : 2;  // only bf16 inputs need the widened copy
-  float Bf[kConvRows * 16];  // B of the stage being consumed, widened to fp32 (bf16 inputs)
+  static constexpr int kConvRows = sizeof(T) == 2 ? TS : 1;  // only bf16 inputs need the widened C
+  float Bf[TS * 16];         // B of the stage being consumed as fp32 (bf16 inputs; structured ZOH: / (n + 1))
   float Cf[kConvRows * 16];  // C of the stage being consumed, widened to fp32 (bf16 inputs)
   unsigned long long fbar[NSF];
   unsigned long long wbar[NSW];
@@ -86,6 +86,7 @@ struct TmaParams {
   const float* delta_bias;  // [D] or null
   const float* D_skip;      // [D] or null
   const void* z;            // [batch, L, D] or null
+  unsigned long long wait_ns;  // bound on one consumer wait (ssm_set_wait_limit_ns)
 };
 
 // ---- PTX wrappers -----------------------------------------------------------------------------------
@@ -112,14 +113,25 @@ __device__ __forceinline__ bool mbar_try(unsigned long long* b, uint32_t parity)
       : "memory");
   return ok != 0;
 }
-// Bounded wait by every lane of the warp; the outcome is warp-uniform. false: the phase did not complete
-// within kWaitNs (the device status word is set).
-__device__ __forceinline__ bool mbar_wait(unsigned long long* b, uint32_t parity) {
-  bool ok = mbar_try(b, parity);
+__device__ __forceinline__ bool mbar_test(unsigned long long* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait by every lane of the warp; the outcome is warp-uniform. One non-blocking probe, then
+// blocking probes until limit_ns have passed. false: the phase did not complete in time (the device
+// status word is set). Consumers pass the launch's limit (ssm_set_wait_limit_ns); the drains before a
+// warp exits pass kWaitNs.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* b, uint32_t parity, unsigned long long limit_ns) {
+  bool ok = mbar_test(b, parity);
   if (!ok) {
     const unsigned long long t0 = gtimer();
-    while (!(ok = mbar_try(b, parity))) {
-      if (gtimer() - t0 > kWaitNs) break;
+    while (gtimer() - t0 < limit_ns) {
+      if ((ok = mbar_try(b, parity))) break;
     }
   }
   ok = __all_sync(0xffffffffu, ok);
@@ -356,11 +368,7 @@ __device__ __forceinline__ void fwd_core(const float2 (&e)[CPL][8], const float2
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const float4 bb = Bq[q], cc = Cq[q];
-    float2 b0 = make_float2(bb.x, bb.y), b1 = make_float2(bb.z, bb.w);
-    if (ZOH) {  // B_n / (n + 1), shared by the CPL channels of the lane
-      b0 = __fmul2_rn(b0, make_float2(1.0f / static_cast<float>(4 * q + 1), 1.0f / static_cast<float>(4 * q + 2)));
-      b1 = __fmul2_rn(b1, make_float2(1.0f / static_cast<float>(4 * q + 3), 1.0f / static_cast<float>(4 * q + 4)));
-    }
+    const float2 b0 = make_float2(bb.x, bb.y), b1 = make_float2(bb.z, bb.w);  // ZOH: already B_n / (n + 1)
     const float2 c0 = make_float2(cc.x, cc.y), c1 = make_float2(cc.z, cc.w);
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
@@ -424,7 +432,7 @@ __device__ __forceinline__ int warm_prologue(WarpRing<T, CPL, TS, NSF, TSW, NSW>
   constexpr int CW = 32 * CPL;
   constexpr uint32_t kWarmBytes = (2u * TSW * CW + TSW * 16) * sizeof(T);
   while (wp.wcon < wp.wiss) {
-    if (!mbar_wait(&r.wbar[wp.wcon % NSW], (wp.wcon / NSW) & 1u)) return -1;
+    if (!mbar_wait(&r.wbar[wp.wcon % NSW], (wp.wcon / NSW) & 1u, kWaitNs)) return -1;
     ++wp.wcon;
   }
   int kiss = 0;
@@ -553,7 +561,7 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
       const int64_t tlo = thi - TSW > 0 ? thi - TSW : 0;
       const int n = static_cast<int>(thi - tlo);
       const int slot = static_cast<int>(wp.wcon % NSW);
-      if (!mbar_wait(&r.wbar[slot], (wp.wcon / NSW) & 1u)) return false;
+      if (!mbar_wait(&r.wbar[slot], (wp.wcon / NSW) & 1u, p.wait_ns)) return false;
       const T* xs = r.wx[slot];
       const T* ds = r.wd[slot];
       const T* Bs = r.wB[slot];
@@ -624,19 +632,32 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
   for (int64_t tb = t0; tb < t1; tb += TS) {
     const int n = static_cast<int>((t1 - tb) < TS ? (t1 - tb) : TS);
     const int slot = static_cast<int>(wp.cseq % NSF);
-    if (!mbar_wait(&r.fbar[slot], (wp.cseq / NSF) & 1u)) return false;
+    if (!mbar_wait(&r.fbar[slot], (wp.cseq / NSF) & 1u, p.wait_ns)) return false;
     const T* xs = r.fx[slot];
     const T* ds = r.fd[slot];
-    if (kConv) {
+    constexpr bool kScaleB = ZOH && S4D;  // the structured ZOH update takes B_n / (n + 1)
+    if constexpr (kConv || kScaleB) {     // this stage's B (and for bf16 inputs C) as fp32, once per stage
+      if constexpr (sizeof(T) == 4) {
+        float4 v = reinterpret_cast<const float4*>(r.fB[slot])[lane];  // entries 4 lane .. 4 lane + 3
+        const int n0 = (4 * lane) & 15;
+        v.x *= 1.0f / static_cast<float>(n0 + 1);
+        v.y *= 1.0f / static_cast<float>(n0 + 2);
+        v.z *= 1.0f / static_cast<float>(n0 + 3);
+        v.w *= 1.0f / static_cast<float>(n0 + 4);
+        reinterpret_cast<float4*>(r.Bf)[lane] = v;
+      } else {
 #pragma unroll
-      for (int j = 0; j < TS * 16 / 32; ++j) {
-        const int i = lane + 32 * j;
-        r.Bf[i] = tof<T>(r.fB[slot][i]);
-        r.Cf[i] = tof<T>(r.fC[slot][i]);
+        for (int j = 0; j < TS * 16 / 32; ++j) {
+          const int i = lane + 32 * j;
+          float bv = tof<T>(r.fB[slot][i]);
+          if (kScaleB) bv *= 1.0f / static_cast<float>((i & 15) + 1);
+          r.Bf[i] = bv;
+          r.Cf[i] = tof<T>(r.fC[slot][i]);
+        }
       }
       __syncwarp();
     }
-    const float* Bs = kConv ? r.Bf : reinterpret_cast<const float*>(r.fB[slot]);
+    const float* Bs = (kConv || kScaleB) ? r.Bf : reinterpret_cast<const float*>(r.fB[slot]);
     const float* Cs = kConv ? r.Cf : reinterpret_cast<const float*>(r.fC[slot]);
     T* yp = static_cast<T*>(p.y) + (b * L + tb) * p.D + d0;  // channel c at yp + 32 c
     const T* zp = EPI == 2 ? static_cast<const T*>(p.z) + (b * L + tb) * p.D + d0 : nullptr;  // gate input
@@ -746,8 +767,12 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
   return true;
 }
 
+// Register budget: the fp32 shape runs 8 warps (up to 255 registers a thread), the bf16 shape 12 (up to
+// 170). Within the fp32 budget the compiler's schedule of the step loop depends on the register count it
+// settles on; a cap of 240 measured fastest on the long ZOH workload (caps from 200 to 255 spread the
+// launch time over about 7%).
 template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int TSW, int NSW, int DX, int EPI>
-__global__ void __launch_bounds__(NW * 32, 1)
+__global__ void __maxnreg__(sizeof(T) == 4 ? 240 : 168)
 scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap md,
                     const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mC,
                     const __grid_constant__ CUtensorMap mxw, const __grid_constant__ CUtensorMap mdw,
@@ -868,11 +893,11 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
 
   // No copy may still be writing this warp's shared memory when the CTA exits.
   while (wp.cseq < iseq) {
-    if (!mbar_wait(&r.fbar[wp.cseq % NSF], (wp.cseq / NSF) & 1u)) break;
+    if (!mbar_wait(&r.fbar[wp.cseq % NSF], (wp.cseq / NSF) & 1u, kWaitNs)) break;
     ++wp.cseq;
   }
   while (wp.wcon < wp.wiss) {
-    if (!mbar_wait(&r.wbar[wp.wcon % NSW], (wp.wcon / NSW) & 1u)) break;
+    if (!mbar_wait(&r.wbar[wp.wcon % NSW], (wp.wcon / NSW) & 1u, kWaitNs)) break;
     ++wp.wcon;
   }
 }
@@ -933,6 +958,7 @@ cudaError_t launch_cfg(const FwdArgs& a) {
   p.D = a.D;
   p.G = (a.D + CW - 1) / CW;
   p.total = a.batch * p.G * a.L;
+  p.wait_ns = wait_limit_ns();
   const size_t smem = sizeof(WarpRing<T, CPL, TS, NSF, TSW, NSW>) * NW + 128;
   auto kern = scan_fwd_tma_kernel<T, ZOH, CPL, NW, TS, NSF, TSW, NSW, DX, EPI>;
   static bool attr_set[64] = {false};

@@ -20,3 +20,14 @@ def pytest_configure(config):
 def orc():
     import oracle
     return oracle.default()
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write every parity comparison (max-norm and elementwise error) to $SSM_PARITY_REPORT, if set."""
+    path = os.environ.get("SSM_PARITY_REPORT")
+    if not path:
+        return
+    import json
+    from tolerance import REPORT
+    with open(path, "w") as f:
+        json.dump([{"test": t, "maxnorm": m, "elementwise": e, "n": n} for t, m, e, n in REPORT], f, indent=0)

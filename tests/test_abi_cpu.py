@@ -150,3 +150,13 @@ def test_ssd_workspace_size(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         _ffi.load(str(tmp_path / "libssm_scan.so"))
+
+
+def test_wait_limit_round_trip(lib):
+    """ssm_set_wait_limit_ns returns the previous bound; the default is 2 s (no GPU work)."""
+    prev = lib.ssm_set_wait_limit_ns(123)
+    try:
+        assert prev == 2_000_000_000
+        assert lib.ssm_set_wait_limit_ns(456) == 123
+    finally:
+        assert lib.ssm_set_wait_limit_ns(prev) == 456

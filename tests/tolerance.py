@@ -2,25 +2,49 @@
 
 The bound is a max-norm relative error: max_i |got_i - ref_i| / max(max_i |ref_i|, 1e-3), at most 1e-4
 for fp32 inputs and 2e-2 for bf16 inputs (fp32 state and accumulation). The elementwise variant
-max_i(|got_i - ref_i| / max(|ref_i|, 1e-3)) is reported alongside; tests/test_tolerance_reading.py shows
-that no fp32 evaluation of the recurrence can meet that variant at 1e-4, so it cannot be the bound.
+max_i(|got_i - ref_i| / max(|ref_i|, 1e-3)) is computed alongside on every comparison and recorded
+(``REPORT``; written as JSON at the end of the session when SSM_PARITY_REPORT names a file);
+tests/test_tolerance_reading.py shows that no fp32 evaluation of the recurrence can meet that variant at
+1e-4, so it cannot be the bound. It still carries a gate of its own, EW_TRIPWIRE: far above what a
+correct kernel shows, it catches an error confined to near-zero outputs that the max-norm would let pass.
 """
+import os
+
 import numpy as np
 
 TOL = {"f32": 1e-4, "bf16": 2e-2}
+# Elementwise tripwire (not the contract's bound): correct fp32 kernels stay within about 1e-2 of it on the
+# smallest outputs (an error of 1e-5 on an output of 1e-3); bf16 outputs carry their own rounding of 2^-9.
+EW_TRIPWIRE = {"f32": 2e-2, "bf16": 2.5e-1}
+
+REPORT = []  # (test id, max-norm error, elementwise error, number of elements)
+
+
+def _pair(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return got, ref
 
 
 def rel_err(got, ref):
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
+    """Max-norm relative error (the gate); the elementwise error of the same pair is recorded in REPORT."""
+    got, ref = _pair(got, ref)
     if ref.size == 0:
         return 0.0
-    return float(np.max(np.abs(got - ref)) / max(float(np.max(np.abs(ref))), 1e-3))
+    diff = np.abs(got - ref)
+    mx = float(np.max(diff) / max(float(np.max(np.abs(ref))), 1e-3))
+    ew = float(np.max(diff / np.maximum(np.abs(ref), 1e-3)))
+    REPORT.append((os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], mx, ew, int(ref.size)))
+    return mx
 
 
 def rel_err_elementwise(got, ref):
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
+    got, ref = _pair(got, ref)
     if ref.size == 0:
         return 0.0
     return float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1e-3)))
+
+
+def last_elementwise():
+    """Elementwise error of the most recent rel_err() comparison."""
+    return REPORT[-1][2] if REPORT else 0.0
