@@ -300,7 +300,8 @@ def measure_prefill(name, reps, flush, peak, fused=False):
     gbs = nbytes / med / 1e9
     what = describe(name, cfg).split(";")[0] + ("; fused softplus(delta + bias), + D x, * SiLU(z)" if fused else "")
     return {"workload": what, "launch_ms_median": med * 1e3, "elems_per_s": b * L * D / med, "gbs": gbs,
-            "hbm_frac": gbs / peak, "bytes_per_launch": nbytes, "reps": reps}
+            "hbm_frac": gbs / peak, "bytes_per_launch": nbytes, "reps": reps,
+            "traffic": None if fused else ncu_traffic("scan_fwd", name)}
 
 
 def measure_backward(name, reps, flush, peak):
