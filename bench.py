@@ -357,13 +357,14 @@ def ssd_bytes(cfg):
     return 2 * b * L * H * P * 2 + 2 * b * L * N * 2 + b * L * H * 4 + H * 4 + b * H * P * N * 4
 
 
-def ssd_flops(cfg, Q=64):
-    """Tensor-core work of the chunked algorithm per launch, per chunk and head: C B^T (2 Q^2 N), the masked
-    product with x (2 Q^2 P), the inter-chunk read-out C S (2 Q N P) and the state update B^T x (2 Q N P),
-    full tiles (the causal halves are counted whole, as a dense evaluation would do them)."""
+def ssd_flops(cfg, Q=128):
+    """Tensor-core work of the chunked algorithm per launch, full tiles (the causal half of the masked product is
+    counted whole, as a dense evaluation does it): per (batch element, chunk) C B^T once (2 Q^2 N; all heads share
+    B and C); per (batch element, chunk, head) the masked product with x (2 Q^2 P), the inter-chunk read-out
+    C S (2 Q N P) and the chunk's state contribution (B^T (w x), 2 Q N P)."""
     b, L, H, P, N = cfg["batch"], cfg["L"], cfg["H"], cfg["P"], cfg["N"]
     chunks = (L + Q - 1) // Q
-    return b * H * chunks * (2 * Q * Q * N + 2 * Q * Q * P + 4 * Q * N * P)
+    return b * chunks * (2 * Q * Q * N + H * (2 * Q * Q * P + 4 * Q * N * P))
 
 
 def measure_ssd(name, reps, flush, peak):
@@ -405,7 +406,7 @@ def measure_ssd(name, reps, flush, peak):
     nbytes, flops = ssd_bytes(cfg), ssd_flops(cfg)
     bf16_peak = measured_tensor_peak()
     return {"workload": f"{name}: Mamba-2 SSD layer, batch {b}, L {L}, {H} heads x {P}, N {N}, bf16, {cfg['disc']}, "
-                        f"chunks of 64", "launch_ms_median": med * 1e3, "elems_per_s": b * L * H * P / med,
+                        f"chunks of 128", "launch_ms_median": med * 1e3, "elems_per_s": b * L * H * P / med,
             "gbs": nbytes / med / 1e9, "hbm_frac": nbytes / med / 1e9 / peak, "bytes_per_launch": nbytes,
             "tflops": flops / med / 1e12, "tensor_frac": flops / med / 1e12 / bf16_peak if bf16_peak else None,
             "flops_per_launch": flops, "workspace_bytes": need, "reps": reps}

@@ -217,7 +217,8 @@ def ssm_ssd_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, want_fin
     """Mamba-2 SSD layer (scalar A per head), CUDA tensors: x [batch, L, H, P] bf16, delta [batch, L, H]
     float32, A_log [H] float32, B, C [batch, L, N] bf16, h0 [batch, H, P, N] float32 or None. Returns
     (y [batch, L, H, P] bf16, final_state [batch, H, P, N] float32 or None). ``workspace``: "auto" allocates
-    the segment workspace here, None runs one CTA per sequence, or a uint8 CUDA tensor."""
+    the workspace here (head dimension 64: the chunk-parallel tensor-core path; otherwise segments of long
+    sequences), None runs the warp-MMA kernel with one CTA per sequence, or a uint8 CUDA tensor."""
     torch = _torch()
     batch, L, H, P = x.shape
     N = B.shape[-1]

@@ -277,9 +277,9 @@ ssm_status ssm_check_device(void* stream) {
   g_last_error[0] = '\0';
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "ssm_check_device");
-  const int st = read_and_clear_device_status();
-  if (st < 0) return fail(SSM_ERR_CUDA, "ssm_check_device: cannot read the device status word");
-  if (st != 0) return fail(SSM_ERR_TIMEOUT, "ssm_check_device: a kernel gave up a bounded wait");
+  const int st = read_and_clear_device_status(), st2 = read_and_clear_ssd_status();
+  if (st < 0 || st2 < 0) return fail(SSM_ERR_CUDA, "ssm_check_device: cannot read the device status word");
+  if (st != 0 || st2 != 0) return fail(SSM_ERR_TIMEOUT, "ssm_check_device: a kernel gave up a bounded wait");
   return SSM_OK;
 }
 

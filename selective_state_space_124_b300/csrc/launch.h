@@ -74,7 +74,7 @@ struct SsdArgs {
   const float* h0;      // [batch, H, P, N] or null
   void* y;              // [batch, L, H, P] bf16
   float* final_state;   // [batch, H, P, N] or null
-  void* workspace;      // ssd_workspace_bytes() bytes for the segmented scan, or null (one CTA per sequence)
+  void* workspace;      // ssd_workspace_bytes() bytes (tensor-core path or segmented scan), or null
   size_t workspace_bytes;
   int64_t batch, L, H, P, N;
   int disc;
@@ -98,5 +98,11 @@ cudaError_t launch_bwd(const BwdArgs& a);
 bool ssd_shape_ok(int64_t P, int64_t N);  // N in {64, 128}, P a multiple of 16
 size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N);  // current device
 cudaError_t launch_ssd(const SsdArgs& a);
+// The tensor-core (tcgen05) SSD path: P = 64, N = 64 or 128, L > 0, with a workspace of
+// ssd_tc_workspace_bytes() (chunk states and the states entering each chunk).
+size_t ssd_tc_workspace_bytes(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N);
+bool ssd_tc_ok(const SsdArgs& a);
+cudaError_t launch_ssd_tc(const SsdArgs& a);
+int read_and_clear_ssd_status();  // nonzero if a kernel of that path recorded a failed bounded wait
 
 }  // namespace ssm

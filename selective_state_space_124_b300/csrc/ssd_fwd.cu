@@ -576,7 +576,7 @@ void ssd_segments(int64_t batch, int64_t L, int64_t H, int64_t P, int* nseg, int
 
 bool ssd_shape_ok(int64_t P, int64_t N) { return (N == 64 || N == 128) && P > 0 && P % kPB == 0; }
 
-size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N) {
+size_t ssd_segment_bytes(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N) {
   int nseg = 1;
   int64_t cps = 1;
   ssd_segments(batch, L, H, P, &nseg, &cps);
@@ -584,7 +584,14 @@ size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H, int64_t P, int64
   return static_cast<size_t>(batch * H * nseg) * static_cast<size_t>(P * N + 1) * sizeof(float);
 }
 
+size_t ssd_workspace_bytes(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N) {
+  const size_t tc = ssd_tc_workspace_bytes(batch, L, H, P, N);
+  if (tc > 0) return tc;  // the tensor-core path takes this shape
+  return ssd_segment_bytes(batch, L, H, P, N);
+}
+
 cudaError_t launch_ssd(const SsdArgs& a) {
+  if (ssd_tc_ok(a)) return launch_ssd_tc(a);
   SsdParams sp;
   sp.x = static_cast<const __nv_bfloat16*>(a.x);
   sp.delta = a.delta;
@@ -600,7 +607,7 @@ cudaError_t launch_ssd(const SsdArgs& a) {
   sp.cps = (a.L + kQ - 1) / kQ;
   sp.seg_state = nullptr;
   sp.seg_logdec = nullptr;
-  const size_t need = ssd_workspace_bytes(a.batch, a.L, a.H, a.P, a.N);
+  const size_t need = ssd_segment_bytes(a.batch, a.L, a.H, a.P, a.N);
   if (need > 0 && a.workspace && a.workspace_bytes >= need) {  // without it, one CTA walks each sequence
     ssd_segments(a.batch, a.L, a.H, a.P, &sp.nseg, &sp.cps);
     if (a.batch * a.H * sp.pblocks * sp.nseg * sp.cps > INT32_MAX) {  // grid too large: one CTA per sequence

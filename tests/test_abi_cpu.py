@@ -139,12 +139,22 @@ def test_ssd_argument_errors(lib):
 
 
 def test_ssd_workspace_size(lib):
-    # segments only where one CTA per sequence (batch x heads x P / 16) leaves SMs idle, each of >= 4 chunks
-    assert lib.ssm_ssd_fwd_workspace_size(8, 4096, 24, 64, 128) == 0    # 768 CTAs: no split
-    assert lib.ssm_ssd_fwd_workspace_size(1, 100, 2, 64, 128) == 0      # 2 chunks: too short to split
-    nbytes = lib.ssm_ssd_fwd_workspace_size(1, 1000, 2, 64, 128)        # 8 CTAs, 16 chunks -> 4 segments
-    assert nbytes == 1 * 2 * 4 * (64 * 128 + 1) * 4
-    assert lib.ssm_ssd_fwd_workspace_size(1, 1000, 2, 64, 96) == 0      # unsupported N
+    # P = 64: the tensor-core path's chunk states (fp32), the states entering each chunk (bf16, rounded up to
+    # 256 bytes) and one log decay per (batch, chunk of 128 steps, head)
+    def tc_bytes(batch, L, H, N):
+        nc = (L + 127) // 128
+        states = batch * nc * H * 64 * N
+        return states * 4 + (states * 2 + 255) // 256 * 256 + batch * nc * H * 4
+    assert lib.ssm_ssd_fwd_workspace_size(8, 4096, 24, 64, 128) == tc_bytes(8, 4096, 24, 128)
+    assert lib.ssm_ssd_fwd_workspace_size(1, 100, 2, 64, 64) == tc_bytes(1, 100, 2, 64)
+    assert lib.ssm_ssd_fwd_workspace_size(1, 0, 2, 64, 128) == 0       # nothing to scan
+    # other P: segments only where one CTA per sequence (batch x heads x P / 16) leaves SMs idle, each of >= 4
+    # chunks of 64 steps
+    assert lib.ssm_ssd_fwd_workspace_size(8, 4096, 24, 32, 128) == 0   # 384 CTAs: no split
+    assert lib.ssm_ssd_fwd_workspace_size(1, 100, 2, 32, 128) == 0     # 2 chunks: too short to split
+    nbytes = lib.ssm_ssd_fwd_workspace_size(1, 1000, 2, 32, 128)       # 4 CTAs, 16 chunks -> 4 segments
+    assert nbytes == 1 * 2 * 4 * (32 * 128 + 1) * 4
+    assert lib.ssm_ssd_fwd_workspace_size(1, 1000, 2, 64, 96) == 0     # unsupported N
 
 
 def test_missing_library_fails_loudly(tmp_path):

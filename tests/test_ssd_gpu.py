@@ -1,7 +1,11 @@
 """Parity of the Mamba-2 SSD layer (ssm_ssd_fwd, chunked, tensor-core products) with the fp64 oracle's plain
 recurrence: both discretisations, with and without an initial state, sequences that end inside a chunk,
 shorter than one chunk and empty, N = 64 and 128, several channel blocks per head, and the full
-Mamba-2-130M-shaped layer."""
+Mamba-2-130M-shaped layer.
+
+Head dimension 64 with a workspace runs the chunk-parallel tcgen05 path (chunks of 128 steps, TMEM
+accumulators, TMA-staged operands); other head dimensions, or no workspace, run the warp-MMA kernel (one CTA
+walking each sequence, optionally in segments). Both are checked here, and against each other."""
 import numpy as np
 import pytest
 
@@ -32,9 +36,10 @@ def _run(orc, batch, L, H, P, N, disc, with_h0, seed, workspace="auto"):
     return y.float().cpu().numpy(), fs.cpu().numpy(), yr, sr
 
 
-# the last shape has 24 heads (384 CTAs: more than two per SM)
+# P = 64 shapes take the tensor-core path: a last chunk of 104 steps (L 1000), 2 steps (L 130), a sequence
+# shorter than one chunk (L 64), an odd head count (the last head pair has one head), exact chunks (L 256)
 SHAPES = [(2, 200, 3, 32, 64), (1, 1000, 2, 64, 128), (2, 64, 1, 16, 128), (1, 7, 2, 16, 64), (1, 130, 1, 48, 128),
-          (4, 130, 24, 64, 64)]
+          (4, 130, 24, 64, 64), (3, 300, 5, 64, 128), (1, 64, 1, 64, 64), (2, 256, 4, 64, 64), (1, 5, 3, 64, 128)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"b{s[0]}_L{s[1]}_H{s[2]}_P{s[3]}_N{s[4]}" for s in SHAPES])
@@ -47,15 +52,16 @@ def test_ssd_parity(orc, shape, disc, with_h0):
     assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
 
 
-# long enough sequences for several segments per sequence (each scanned by its own CTAs, then fixed up)
-SEG_SHAPES = [(1, 1000, 2, 64, 128), (1, 700, 1, 16, 64), (2, 2048, 3, 32, 128)]
+# with the workspace: the tensor-core path (P = 64) or segments per sequence (each scanned by its own CTAs, then
+# fixed up); without it: one CTA per sequence
+SEG_SHAPES = [(1, 1000, 2, 64, 128), (1, 700, 1, 16, 64), (2, 2048, 3, 32, 128), (2, 2048, 3, 64, 64)]
 
 
 @pytest.mark.parametrize("shape", SEG_SHAPES, ids=[f"b{s[0]}_L{s[1]}_H{s[2]}_P{s[3]}_N{s[4]}" for s in SEG_SHAPES])
 @pytest.mark.parametrize("disc", ["euler", "zoh"])
 @pytest.mark.parametrize("with_h0", [False, True], ids=["zero_state", "h0"])
 def test_ssd_segments_match_one_cta_per_sequence(orc, shape, disc, with_h0):
-    """With and without the segment workspace: both against the oracle, and the segmented run really splits."""
+    """With and without the workspace: both against the oracle (a workspace is offered for every such shape)."""
     import selective_state_space_124_b300 as lib
     assert lib.ssd_workspace_size(shape[0], shape[1], shape[2], shape[3], shape[4]) > 0
     for ws in ("auto", None):
@@ -94,3 +100,28 @@ def test_ssd_rejects_unsupported_shapes():
     Bm = torch.zeros((1, 8, 32), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(lib.SsmError, match="N = 64 or 128"):
         lib.ssm_ssd_fwd(x, torch.zeros((1, 8, 1), device="cuda"), torch.zeros(1, device="cuda"), Bm, Bm)
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+def test_ssd_tensor_core_path_matches_warp_mma_path(orc, disc):
+    """P = 64: the tcgen05 path (with workspace) and the warp-MMA kernel (without) give the same layer within the
+    bf16 tolerance of each other, on a layer of several chunks, heads and batch elements with an initial state."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    batch, L, H, P, N = 2, 700, 6, 64, 128
+    inp = ssm_inputs.make_ssd_inputs(batch, L, H, P, N, seed=71)
+    h0 = torch.from_numpy(np.random.default_rng(72).standard_normal((batch, H, P, N)).astype(np.float32)).cuda()
+    x = _bf16(torch, inp["x_bits"], (batch, L, H, P))
+    B = _bf16(torch, inp["B_bits"], (batch, L, N))
+    C = _bf16(torch, inp["C_bits"], (batch, L, N))
+    dt = torch.from_numpy(inp["delta"]).cuda()
+    A = torch.from_numpy(inp["A_log"]).cuda()
+    assert lib.ssd_workspace_size(batch, L, H, P, N) > 0
+    y1, f1 = lib.ssm_ssd_fwd(x, dt, A, B, C, disc=disc, h0=h0, workspace="auto")
+    y2, f2 = lib.ssm_ssd_fwd(x, dt, A, B, C, disc=disc, h0=h0, workspace=None)
+    lib.check_device()
+    assert rel_err(y1.float().cpu().numpy(), y2.float().cpu().numpy()) <= TOL["bf16"]
+    assert rel_err(f1.cpu().numpy(), f2.cpu().numpy()) <= TOL["bf16"]
+    yr, sr = orc.ssd_fwd(inp["x"], inp["delta"], inp["A_log"], inp["B"], inp["C"], disc=disc, h0=h0.cpu().numpy())
+    assert rel_err(y1.float().cpu().numpy(), yr) <= TOL["bf16"]
+    assert rel_err(f1.cpu().numpy(), sr) <= TOL["bf16"]
