@@ -60,8 +60,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the other workloads (reported under 'workloads')")
     ap.add_argument("--profile", action="store_true",
-                    help="a lean run for profilers: no L2-flush buffers, no other workloads, no end-to-end leg, "
-                         "no CPU baseline (its timings are not benchmark values)")
+                    help="a lean run for profilers: no L2-flush buffers, no end-to-end leg, no CPU baseline, other "
+                         "workloads only if --extra names them (its timings are not benchmark values)")
     ap.add_argument("--extra", default="all", metavar="KIND[,KIND]",
                     help="which other workloads to time: all, or any of prefill, fused, bwd, ssd, decode")
     return ap.parse_args(argv)
@@ -643,8 +643,9 @@ def main(argv=None):
     y = torch.empty((b, L, D), dtype=tdt, device="cuda")
     state = torch.empty((b, D, N), dtype=torch.float32, device="cuda")
     y_t = torch.empty((b, D), dtype=tdt, device="cuda")
-    if args.profile:
-        args.no_extra = args.no_e2e = args.no_cpu_baseline = True
+    if args.profile:  # other workloads only when --extra names them
+        args.no_e2e = args.no_cpu_baseline = True
+        args.no_extra = args.no_extra or args.extra == "all"
     flush = torch.empty(FLUSH_BYTES // 4 if not args.profile else 256, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 

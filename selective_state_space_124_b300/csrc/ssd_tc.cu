@@ -154,16 +154,27 @@ struct TcParams {
 
 // Per-step log decay s (inclusive running sum of delta A over the chunk) and input coefficient, one warp for one
 // head: lane l takes steps 4 l .. 4 l + 3. Steps past L take delta = 0.
+// The deltas of steps 4 lane .. 4 lane + 3 of chunk c for head h (0 past L). Loaded before a CTA issues its bulk
+// copies, so that these small loads do not queue behind them.
+__device__ __forceinline__ void load_deltas(const TcParams& p, int64_t b, int64_t c, int64_t h, int lane, float (&d)[4],
+                                            float& alog) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int64_t t = c * kTQ + 4 * lane + k;
+    d[k] = t < p.L ? __ldg(p.delta + (b * p.L + t) * p.H + h) : 0.0f;
+  }
+  alog = __ldg(p.A_log + h);
+}
+
 template <bool ZOH>
-__device__ __forceinline__ void chunk_decays(const TcParams& p, int64_t b, int64_t c, int64_t h, int lane, float (&s)[4],
-                                             float (&cf)[4], float& s_last) {
-  const float A = -ex2(__ldg(p.A_log + h) * kLog2e);
+__device__ __forceinline__ void chunk_decays(const float (&dv)[4], float alog, int lane, float (&s)[4], float (&cf)[4],
+                                             float& s_last) {
+  const float A = -ex2(alog * kLog2e);
   const float A2 = A * kLog2e;
   float a[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int64_t t = c * kTQ + 4 * lane + k;
-    const float d = t < p.L ? __ldg(p.delta + (b * p.L + t) * p.H + h) : 0.0f;
+    const float d = dv[k];
     a[k] = d * A;
     if (ZOH) {
       const float w = d * A2;
@@ -220,6 +231,8 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
   const uint32_t tmem = sm.tmem;
   // Outstanding asynchronous work (thread 0's view): the phase each barrier still owes, or -1.
   int pendB = -1, pendX = -1, pendM = -1;
+  float dv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, alog = 0.0f;  // warps 0, 1: the first pair's deltas (loaded first)
+  if (warp < 2 && 2 * g * kPairsPerCta + warp < p.H) load_deltas(p, b, c, 2 * g * kPairsPerCta + warp, lane, dv, alog);
   if (tid == 0) {
     mb_expect(&sm.barB, N * 256);
 #pragma unroll
@@ -242,8 +255,9 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
     if (warp < 2) {  // warp 0: head h0, warp 1: head h0 + 1
       const int64_t h = h0 + warp;
       if (h < p.H) {
+        if (q > 0) load_deltas(p, b, c, h, lane, dv, alog);
         float s[4], cf[4], s_last;
-        chunk_decays<ZOH>(p, b, c, h, lane, s, cf, s_last);
+        chunk_decays<ZOH>(dv, alog, lane, s, cf, s_last);
 #pragma unroll
         for (int k = 0; k < 4; ++k) sm.w[warp][4 * lane + k] = ex2((s_last - s[k]) * kLog2e) * cf[k];
         if (lane == 0) p.slast[(b * p.nc + c) * p.H + h] = s_last;
@@ -330,38 +344,45 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
 // ---- launch 2: the recurrence between chunks ---------------------------------------------------------------
 // One thread per (b, h, p, 4 consecutive n).
 template <int N>
-__global__ void __launch_bounds__(256) ssd_state_pass_kernel(TcParams p) {
+__global__ void __launch_bounds__(256, 4) ssd_state_pass_kernel(TcParams p) {
   const int64_t total = p.batch * p.H * kTP * (N / 4);
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= total) return;
   const int64_t n4 = i % (N / 4), pp = (i / (N / 4)) % kTP, h = (i / (N / 4) / kTP) % p.H, b = i / (N / 4) / kTP / p.H;
   const int64_t row = (b * p.H + h) * kTP + pp;  // (b, h, p) of h0 / final_state
   float4 s = p.h0 ? *reinterpret_cast<const float4*>(p.h0 + row * N + 4 * n4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  // (b, c, h, p) rows of E / S and (b, c, h) entries of slast step by H * 64 rows and H entries per chunk
+  const float* ep = p.E + ((b * p.nc * p.H + h) * kTP + pp) * N + 4 * n4;
+  __nv_bfloat16* sp = p.S + ((b * p.nc * p.H + h) * kTP + pp) * N + 4 * n4;
+  const float* dp = p.slast + b * p.nc * p.H + h;
+  const int64_t estep = p.H * kTP * N;
   constexpr int kAhead = 8;  // chunks whose E and decay are loaded together, ahead of the dependent updates
   for (int64_t c0 = 0; c0 < p.nc; c0 += kAhead) {
+    const int n = p.nc - c0 < kAhead ? static_cast<int>(p.nc - c0) : kAhead;
     float4 e[kAhead];
     float dl[kAhead];
 #pragma unroll
     for (int k = 0; k < kAhead; ++k) {
-      if (c0 + k < p.nc) {
-        const int64_t at = ((b * p.nc + c0 + k) * p.H + h) * kTP + pp;  // (b, c, h, p) of E / S
-        e[k] = *reinterpret_cast<const float4*>(p.E + at * N + 4 * n4);
-        dl[k] = p.slast[(b * p.nc + c0 + k) * p.H + h];
+      if (k < n) {
+        e[k] = *reinterpret_cast<const float4*>(ep + k * estep);
+        dl[k] = dp[k * p.H];
       }
     }
 #pragma unroll
     for (int k = 0; k < kAhead; ++k) {
-      if (c0 + k < p.nc) {
-        const int64_t at = ((b * p.nc + c0 + k) * p.H + h) * kTP + pp;
+      if (k < n) {
         uint2 packed;
         packed.x = bf2(s.x, s.y);
         packed.y = bf2(s.z, s.w);
-        *reinterpret_cast<uint2*>(p.S + at * N + 4 * n4) = packed;
+        *reinterpret_cast<uint2*>(sp + k * estep) = packed;
         const float dec = ex2(dl[k] * kLog2e);
         s = make_float4(fmaf(dec, s.x, e[k].x), fmaf(dec, s.y, e[k].y), fmaf(dec, s.z, e[k].z),
                         fmaf(dec, s.w, e[k].w));
       }
     }
+    ep += kAhead * estep;
+    sp += kAhead * estep;
+    dp += kAhead * p.H;
   }
   if (p.final_state) *reinterpret_cast<float4*>(p.final_state + row * N + 4 * n4) = s;
 }
@@ -409,6 +430,8 @@ __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__
   const int half = warp >> 2;  // which half of the columns this warp takes
   // Outstanding asynchronous work (thread 0's view): the phase each barrier still owes, or -1.
   int pendCB = -1, pendXS = -1, pendG = -1, pendM = -1;
+  float dv[4] = {0.0f, 0.0f, 0.0f, 0.0f}, alog = 0.0f;  // warp w < nh: deltas of head hbase + w (loaded first)
+  if (warp < nh) load_deltas(p, b, c, hbase + warp, lane, dv, alog);
   auto issue_xs = [&](int64_t h, uint32_t ph) {  // x tile and S_c of head h (thread 0)
     mb_expect(&sm.barXS, kXSBytes);
     tma3(sm.Xt, &mX, static_cast<int>(h * kTP), static_cast<int>(c * kTQ), static_cast<int>(b), &sm.barXS);
@@ -429,7 +452,7 @@ __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__
   }
   if (warp < nh) {  // warp w: decays of head hbase + w
     float s[4], cf[4], s_last;
-    chunk_decays<ZOH>(p, b, c, hbase + warp, lane, s, cf, s_last);
+    chunk_decays<ZOH>(dv, alog, lane, s, cf, s_last);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       sm.s[warp][4 * lane + k] = s[k] * kLog2e;
