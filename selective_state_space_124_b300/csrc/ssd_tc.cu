@@ -122,16 +122,21 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
 __device__ __forceinline__ void mma_commit(unsigned long long* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s32(bar)) : "memory");
 }
-// 16 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32 w .. 32 w + 31).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32 (w % 4) .. + 31), without
+// waiting: the registers are valid after tmem_wait().
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
       "[%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  tmem_ld16_async(taddr, r);
+  tmem_wait();
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -314,14 +319,20 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
       const int m = (warp & 3) * 32 + lane;
       const int64_t h = h0 + (m >> 6);
       float* out = p.E + (((b * p.nc + c) * p.H + h) * kTP + (m & 63)) * N;
+      uint32_t v[N / 32][16];  // this thread's N / 2 columns: all loads, then one wait
 #pragma unroll
-      for (int c0 = (warp >> 2) * (N / 2); c0 < (warp >> 2) * (N / 2) + N / 2; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + c0, v);
-        if (h < p.H) {
+      for (int k = 0; k < N / 32; ++k)
+        tmem_ld16_async(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + (warp >> 2) * (N / 2) + 16 * k, v[k]);
+      tmem_wait();
+      if (h < p.H) {
+#pragma unroll
+        for (int k = 0; k < N / 32; ++k) {
+          const int c0 = (warp >> 2) * (N / 2) + 16 * k;
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(out + c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            *reinterpret_cast<float4*>(out + c0 + e) =
+                make_float4(__uint_as_float(v[k][e]), __uint_as_float(v[k][e + 1]), __uint_as_float(v[k][e + 2]),
+                            __uint_as_float(v[k][e + 3]));
         }
       }
     }
@@ -490,24 +501,26 @@ __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__
       const float si = sm.s[q][i];
       const float4* s4 = reinterpret_cast<const float4*>(sm.s[q]);
       const float4* c4 = reinterpret_cast<const float4*>(sm.cf[q]);
-#pragma unroll 1
-      for (int j0 = half * 64; j0 < half * 64 + 64; j0 += 16) {
+      uint32_t graw[4][16];  // G[i][j] for this thread's 64 columns, four loads and one wait
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) tmem_ld16_async(tmem + lane_base + half * 64 + 16 * g4, graw[g4]);
+      tmem_wait();
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) {
+        const int j0 = half * 64 + 16 * g4;
         uint32_t pk[8];
-        if (j0 > i) {  // the whole group lies above the diagonal (warp-uniform only per row: lanes differ)
+        if (j0 > i) {  // the whole group lies above the diagonal
 #pragma unroll
           for (int e = 0; e < 8; ++e) pk[e] = 0u;
-        }
-        float gv[16];
-        tmem_ld16(tmem + lane_base + j0, gv);  // every lane of the warp takes part in the load
-        if (j0 <= i) {
+        } else {
 #pragma unroll
           for (int e4 = 0; e4 < 4; ++e4) {
             const float4 sj = s4[j0 / 4 + e4], cj = c4[j0 / 4 + e4];
             const int j = j0 + 4 * e4;
-            const float m0 = j <= i ? gv[4 * e4] * ex2(si - sj.x) * cj.x : 0.0f;
-            const float m1 = j + 1 <= i ? gv[4 * e4 + 1] * ex2(si - sj.y) * cj.y : 0.0f;
-            const float m2 = j + 2 <= i ? gv[4 * e4 + 2] * ex2(si - sj.z) * cj.z : 0.0f;
-            const float m3 = j + 3 <= i ? gv[4 * e4 + 3] * ex2(si - sj.w) * cj.w : 0.0f;
+            const float m0 = j <= i ? __uint_as_float(graw[g4][4 * e4]) * ex2(si - sj.x) * cj.x : 0.0f;
+            const float m1 = j + 1 <= i ? __uint_as_float(graw[g4][4 * e4 + 1]) * ex2(si - sj.y) * cj.y : 0.0f;
+            const float m2 = j + 2 <= i ? __uint_as_float(graw[g4][4 * e4 + 2]) * ex2(si - sj.z) * cj.z : 0.0f;
+            const float m3 = j + 3 <= i ? __uint_as_float(graw[g4][4 * e4 + 3]) * ex2(si - sj.w) * cj.w : 0.0f;
             pk[2 * e4] = bf2(m0, m1);
             pk[2 * e4 + 1] = bf2(m2, m3);
           }
@@ -553,14 +566,21 @@ __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__
     {
       const float e = ex2(sm.s[q][i]);
       __nv_bfloat16* yp = p.y + ((b * p.L + t) * p.H + h) * kTP;
+      uint32_t d1[2][16], d2[2][16];  // this thread's 32 columns of D1 and D2: four loads, one wait
 #pragma unroll
-      for (int p0 = half * (kTP / 2); p0 < half * (kTP / 2) + kTP / 2; p0 += 16) {
-        float d1[16], d2[16];
-        tmem_ld16(tmem + lane_base + 128 + p0, d1);
-        tmem_ld16(tmem + lane_base + 192 + p0, d2);
+      for (int k = 0; k < 2; ++k) {
+        tmem_ld16_async(tmem + lane_base + 128 + half * (kTP / 2) + 16 * k, d1[k]);
+        tmem_ld16_async(tmem + lane_base + 192 + half * (kTP / 2) + 16 * k, d2[k]);
+      }
+      tmem_wait();
+#pragma unroll
+      for (int k2 = 0; k2 < 2; ++k2) {
+        const int p0 = half * (kTP / 2) + 16 * k2;
         uint32_t pk[8];
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) pk[k / 2] = bf2(fmaf(e, d2[k], d1[k]), fmaf(e, d2[k + 1], d1[k + 1]));
+        for (int k = 0; k < 16; k += 2)
+          pk[k / 2] = bf2(fmaf(e, __uint_as_float(d2[k2][k]), __uint_as_float(d1[k2][k])),
+                          fmaf(e, __uint_as_float(d2[k2][k + 1]), __uint_as_float(d1[k2][k + 1])));
         if (t < p.L) {
           *reinterpret_cast<uint4*>(yp + p0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           *reinterpret_cast<uint4*>(yp + p0 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
