@@ -743,7 +743,8 @@ def main(argv=None):
         "dtype": cfg["dtype"], "data": "synthetic",
         "config": config,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic("scan_fwd", args.workload),
+                     "frac": achieved / peak,
+                     "traffic": None if overrides else ncu_traffic("scan_fwd", args.workload),
                      "peak_kind": peak_kind, "kernel": "ssm_scan_fwd",
                      "algorithmic_bytes_per_launch": fwd_bytes(cfg), "avg_launch_ms": fwd_avg_s * 1e3},
         "fwd_ms_median": statistics.median(fwd_ms), "step_ms_median": statistics.median(stp_ms),
