@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "pair_math.cuh"
 
 namespace ssm {
 namespace {
@@ -394,6 +395,439 @@ __device__ __forceinline__ void bwd_piece(const BwdParams& p, const BwdChan<NP, 
   }
 }
 
+// ---- structured A (N = 16, A_n = (n + 1) A_0 on every channel of the warp) ------------------------------
+// The same four phases, two state entries per f32x2 instruction, with the per-step algebra cut down:
+//   * one decay tree e_0 -> e_1 .. e_15 per step (exact identity, one SFU exp2);
+//   * the decayed previous state u_n = Abar_n h_{t-1,n} is formed once and serves both dA_n (sum of
+//     delta lambda u) and ddelta's decay term (sum of A_n lambda u);
+//   * Euler: dx and ddelta's input term share sigma = sum_n lambda_n B_n (dx = delta sigma, + x sigma);
+//   * the walks drop state pairs once their weight is below the truncation bound on every lane (entry n
+//     decays (n + 1) times as fast as entry 0);
+//   * dB and dC, sums over the warp's channels, go through a transposition tile in shared memory (each lane
+//     writes its 32 terms as a row, reads a column and adds it up) instead of a shuffle tree;
+//   * the next chunk's inputs are loaded into registers while the current chunk is computed.
+// Per-warp shared memory (floats): hs [kChunk][8 pairs][32 lanes] float2, the state before each step of the
+// chunk being differentiated; hst [8][32] float2, the state entering the piece; xs, ds, gs [kChunk][32];
+// bs, cs [kChunk][16]; red [32][32], the transposition tile.
+constexpr int kS4dWarpFloats = kChunk * 512 + 512 + 3 * kChunk * 32 + 2 * kChunk * 16 + 1024;
+
+// 2k + 1 and 2k + 2: entry n's decay rate is (n + 1) times entry 0's
+__constant__ float2 kPairN1[8] = {{1.f, 2.f},   {3.f, 4.f},   {5.f, 6.f},   {7.f, 8.f},
+                                  {9.f, 10.f},  {11.f, 12.f}, {13.f, 14.f}, {15.f, 16.f}};
+__constant__ float2 kPairInvN1[8] = {{1.f, 1.f / 2.f},         {1.f / 3.f, 1.f / 4.f},   {1.f / 5.f, 1.f / 6.f},
+                                     {1.f / 7.f, 1.f / 8.f},   {1.f / 9.f, 1.f / 10.f},  {1.f / 11.f, 1.f / 12.f},
+                                     {1.f / 13.f, 1.f / 14.f}, {1.f / 15.f, 1.f / 16.f}};
+
+// A chunk's inputs held in registers between their load and their store to shared memory, so that the loads
+// of the next chunk are in flight while the current one is computed.
+struct ChunkRegs {
+  float x[kChunk], d[kChunk], g[kChunk], b[kChunk * 16 / 32], c[kChunk * 16 / 32];
+};
+
+template <typename T, bool WX, bool WG, bool WB, bool WC>
+__device__ __forceinline__ void chunk_load(const BwdParams& p, int64_t b, int64_t d, bool act, int lane, int64_t s,
+                                           int n, ChunkRegs& r) {
+  const int64_t base = (b * p.L + s) * p.D + d;
+  const int64_t bc = (b * p.L + s) * 16;
+#pragma unroll
+  for (int i = 0; i < kChunk; ++i) {
+    const bool ok = act && i < n;
+    if (WX) r.x[i] = ok ? Elem<T>::load(p.x, base + static_cast<int64_t>(i) * p.D) : 0.0f;
+    r.d[i] = ok ? Elem<T>::load(p.delta, base + static_cast<int64_t>(i) * p.D) : 0.0f;
+    if (WG) r.g[i] = ok ? Elem<T>::load(p.dy, base + static_cast<int64_t>(i) * p.D) : 0.0f;
+  }
+#pragma unroll
+  for (int m = 0; m < kChunk * 16 / 32; ++m) {
+    const int k = lane + 32 * m;
+    const bool ok = (k >> 4) < n;
+    if (WB) r.b[m] = ok ? Elem<T>::load(p.B, bc + k) : 0.0f;
+    if (WC) r.c[m] = ok ? Elem<T>::load(p.C, bc + k) : 0.0f;
+  }
+}
+
+template <bool WX, bool WG, bool WB, bool WC>
+__device__ __forceinline__ void chunk_store(const ChunkRegs& r, int lane, float* xs, float* ds, float* gs, float* bs,
+                                            float* cs) {
+  __syncwarp();  // every lane has finished reading the previous chunk
+#pragma unroll
+  for (int i = 0; i < kChunk; ++i) {
+    if (WX) xs[i * 32 + lane] = r.x[i];
+    ds[i * 32 + lane] = r.d[i];
+    if (WG) gs[i * 32 + lane] = r.g[i];
+  }
+#pragma unroll
+  for (int m = 0; m < kChunk * 16 / 32; ++m) {
+    if (WB) bs[lane + 32 * m] = r.b[m];
+    if (WC) cs[lane + 32 * m] = r.c[m];
+  }
+  __syncwarp();
+}
+
+// Phase 1 over one staged chunk, steps cn - 1 .. 0, with the first ACT pairs live. W: log2 of entry 0's decay
+// over the steps after the current one; P: the live pairs' weights. ZOH accumulates P e B x / A_0; the 1/(n+1)
+// of Bbar is applied once when the walk ends.
+template <int ACT, bool ZOH>
+__device__ __forceinline__ void s4d_walk_back(const float* xs, const float* ds, const float* bs, int cn, int lane,
+                                              float A2_0, float invA0, float& W, float2 (&P)[8], float2 (&h)[8]) {
+  using namespace pairs;
+#pragma unroll 1
+  for (int i = cn - 1; i >= 0; --i) {
+    const float xv = xs[i * 32 + lane], dv = ds[i * 32 + lane];
+    const float2* brow = reinterpret_cast<const float2*>(bs + i * 16);
+    const float w = dv * A2_0;
+    if (ZOH) {
+      float2 e[8];
+      em1_tree<ACT>(exp2m1(w, ex2(w)), e);
+      const float2 xi = bc(xv * invA0);
+#pragma unroll
+      for (int k = 0; k < ACT; ++k) h[k] = fma2(mul2(P[k], e[k]), mul2(brow[k], xi), h[k]);
+    } else {
+      const float2 u = bc(dv * xv);
+#pragma unroll
+      for (int k = 0; k < ACT; ++k) h[k] = fma2(P[k], mul2(brow[k], u), h[k]);
+    }
+    W += w;
+    powers<ACT>(ex2(W), P);
+  }
+}
+
+// Phase 3 over one staged chunk, steps 0 .. cn - 1: mu_n += (decay of entry n from t1 through the step)
+// C_n dy. W: log2 of entry 0's decay from t1 through the current step.
+template <int ACT>
+__device__ __forceinline__ void s4d_walk_fwd(const float* ds, const float* gs, const float* cs, int cn, int lane,
+                                             float A2_0, float& W, float2 (&P)[8], float2 (&mu)[8]) {
+  using namespace pairs;
+#pragma unroll 1
+  for (int i = 0; i < cn; ++i) {
+    W = fmaf(ds[i * 32 + lane], A2_0, W);
+    powers<ACT>(ex2(W), P);
+    const float2 g = bc(gs[i * 32 + lane]);
+    const float2* crow = reinterpret_cast<const float2*>(cs + i * 16);
+#pragma unroll
+    for (int k = 0; k < ACT; ++k) mu[k] = fma2(P[k], mul2(crow[k], g), mu[k]);
+  }
+}
+
+// One forward step of the structured recurrence on all 16 entries (the forward kernels' update):
+// Euler h + e h + (delta x) B; ZOH h + e (h + (x / A_0) B / (n + 1)).
+template <bool ZOH>
+__device__ __forceinline__ void s4d_fwd_step(float xv, float dv, const float* brow_f, float A2_0, float invA0,
+                                             float2 (&h)[8]) {
+  using namespace pairs;
+  const float2* brow = reinterpret_cast<const float2*>(brow_f);
+  float2 e[8];
+  step_e16(dv * A2_0, e);
+  if (ZOH) {
+    const float2 s = bc(xv * invA0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[k] = fma2(e[k], fma2(mul2(brow[k], kPairInvN1[k]), s, h[k]), h[k]);
+  } else {
+    const float2 s = bc(dv * xv);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[k] = fma2(s, brow[k], fma2(e[k], h[k], h[k]));
+  }
+}
+
+// f(w) = (w e^w - (e^w - 1)) / w^2 for a pair (ZOH dBbar/dA = B delta^2 f(delta A)): its Taylor series where
+// the difference would cancel (|w| < 1/4), the difference itself elsewhere; a = e^w, e = e^w - 1.
+__device__ __forceinline__ float2 zoh_f2(float2 w, float2 a, float2 e) {
+  using namespace pairs;
+  float2 q = fma2(w, bc(1.0f / 5760.0f), bc(1.0f / 840.0f));
+  q = fma2(w, q, bc(1.0f / 144.0f));
+  q = fma2(w, q, bc(1.0f / 30.0f));
+  q = fma2(w, q, bc(1.0f / 8.0f));
+  q = fma2(w, q, bc(1.0f / 3.0f));
+  q = fma2(w, q, bc(0.5f));
+  const float2 num = fma2(w, a, make_float2(-e.x, -e.y));
+  const float2 w2 = mul2(w, w);
+  return make_float2(fabsf(w.x) < 0.25f ? q.x : num.x * rcp_approx(w2.x),
+                     fabsf(w.y) < 0.25f ? q.y : num.y * rcp_approx(w2.y));
+}
+
+template <bool ZOH, typename T>
+__device__ __forceinline__ void bwd_piece_s4d(const BwdParams& p, float A0, float* wsm, int lane, int64_t row,
+                                              int64_t t0, int64_t t1) {
+  using namespace pairs;
+  float2* hs = reinterpret_cast<float2*>(wsm);             // [kChunk][8][32]
+  float2* hst = hs + kChunk * 8 * 32;                       // [8][32]
+  float* xs = reinterpret_cast<float*>(hst + 8 * 32);
+  float* ds = xs + kChunk * 32;
+  float* gs = ds + kChunk * 32;
+  float* bs = gs + kChunk * 32;
+  float* cs = bs + kChunk * 16;
+  float* red = cs + kChunk * 16;                            // [32][32]
+  const int64_t L = p.L, D = p.D;
+  const int64_t b = row / p.groups;
+  const int64_t d = (row % p.groups) * 32 + lane;
+  const bool act = d < D;
+  const float A2_0 = A0 * kLog2e, invA0 = 1.0f / A0;
+  ChunkRegs nx;
+
+  // ---- 1. h(t0 - 1) by the truncated backward walk ---------------------------------------------------
+  float2 h[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) h[k] = make_float2(0.0f, 0.0f);
+  const float* h0row = p.h0 ? p.h0 + (b * D + d) * 16 : nullptr;
+  if (t0 > 0) {
+    float W = 0.0f;
+    float2 P[8];
+    powers<8>(1.0f, P);
+    int live = 8;
+    int64_t j = t0;
+    int64_t s = j > kChunk ? j - kChunk : 0;
+    chunk_load<T, true, false, true, false>(p, b, d, act, lane, s, static_cast<int>(j - s), nx);
+    while (true) {  // chunk [s, j)
+      const int cn = static_cast<int>(j - s);
+      chunk_store<true, false, true, false>(nx, lane, xs, ds, gs, bs, cs);
+      const int64_t s2 = s > kChunk ? s - kChunk : 0;
+      if (s > 0) chunk_load<T, true, false, true, false>(p, b, d, act, lane, s2, static_cast<int>(s - s2), nx);
+      if (live == 8) s4d_walk_back<8, ZOH>(xs, ds, bs, cn, lane, A2_0, invA0, W, P, h);
+      else if (live == 4) s4d_walk_back<4, ZOH>(xs, ds, bs, cn, lane, A2_0, invA0, W, P, h);
+      else if (live == 2) s4d_walk_back<2, ZOH>(xs, ds, bs, cn, lane, A2_0, invA0, W, P, h);
+      else s4d_walk_back<1, ZOH>(xs, ds, bs, cn, lane, A2_0, invA0, W, P, h);
+      j = s;
+      s = s2;
+      if (j == 0) break;
+      const int l2 = live_pairs(warp_max_f(act ? ex2(W) : 0.0f));
+      if (l2 == 0) break;
+      live = l2 < live ? l2 : live;  // a dropped pair's weights are no longer updated: never revive one
+    }
+    if (ZOH) {  // the walk summed P e B x / A_0: Bbar_n x = e_n B_n x / ((n + 1) A_0)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) h[k] = mul2(h[k], kPairInvN1[k]);
+    }
+    if (j == 0 && h0row && act) {  // the walk reached t = 0: add the initial state, decayed through t0 - 1
+      powers<8>(ex2(W), P);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) h[k] = fma2(P[k], make_float2(h0row[2 * k], h0row[2 * k + 1]), h[k]);
+    }
+  } else if (h0row && act) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[k] = make_float2(h0row[2 * k], h0row[2 * k + 1]);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) hst[k * 32 + lane] = h[k];
+
+  // ---- 2. forward over the piece in aligned chunks, saving the state at each chunk end followed by another
+  {
+    const int64_t ck0 = t0 / kChunk, ck1 = (t1 - 1) / kChunk;
+    auto span = [&](int64_t ck, int64_t& s, int64_t& e) {
+      s = ck * kChunk > t0 ? ck * kChunk : t0;
+      e = (ck + 1) * kChunk < t1 ? (ck + 1) * kChunk : t1;
+    };
+    int64_t s, e;
+    span(ck0, s, e);
+    chunk_load<T, true, false, true, false>(p, b, d, act, lane, s, static_cast<int>(e - s), nx);
+    for (int64_t ck = ck0; ck <= ck1; ++ck) {
+      span(ck, s, e);
+      chunk_store<true, false, true, false>(nx, lane, xs, ds, gs, bs, cs);
+      if (ck < ck1) {
+        int64_t s2, e2;
+        span(ck + 1, s2, e2);
+        chunk_load<T, true, false, true, false>(p, b, d, act, lane, s2, static_cast<int>(e2 - s2), nx);
+      }
+      const int cn = static_cast<int>(e - s);
+#pragma unroll 1
+      for (int i = 0; i < cn; ++i) s4d_fwd_step<ZOH>(xs[i * 32 + lane], ds[i * 32 + lane], bs + i * 16, A2_0, invA0, h);
+      if (ck < ck1 && act) {  // chunk ck ends inside the piece
+        float* w = p.ws + ((b * p.nck + ck) * 16) * D + d;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          w[static_cast<int64_t>(2 * k) * D] = h[k].x;
+          w[static_cast<int64_t>(2 * k + 1) * D] = h[k].y;
+        }
+      }
+    }
+  }
+
+  // ---- 3. the adjoint entering from the right of the piece: forward walk from t1 ---------------------------
+  float2 mu[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mu[k] = make_float2(0.0f, 0.0f);
+  const float* dfrow = p.dfinal ? p.dfinal + (b * D + d) * 16 : nullptr;
+  if (t1 == L) {
+    if (dfrow && act) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mu[k] = make_float2(dfrow[2 * k], dfrow[2 * k + 1]);
+    }
+  } else {
+    float W = 0.0f;
+    float2 P[8];
+    powers<8>(1.0f, P);
+    int live = 8;
+    int64_t j = t1;
+    int64_t e = j + kChunk < L ? j + kChunk : L;
+    chunk_load<T, false, true, false, true>(p, b, d, act, lane, j, static_cast<int>(e - j), nx);
+    while (true) {  // chunk [j, e)
+      const int cn = static_cast<int>(e - j);
+      chunk_store<false, true, false, true>(nx, lane, xs, ds, gs, bs, cs);
+      const int64_t e2 = e + kChunk < L ? e + kChunk : L;
+      if (e < L) chunk_load<T, false, true, false, true>(p, b, d, act, lane, e, static_cast<int>(e2 - e), nx);
+      if (live == 8) s4d_walk_fwd<8>(ds, gs, cs, cn, lane, A2_0, W, P, mu);
+      else if (live == 4) s4d_walk_fwd<4>(ds, gs, cs, cn, lane, A2_0, W, P, mu);
+      else if (live == 2) s4d_walk_fwd<2>(ds, gs, cs, cn, lane, A2_0, W, P, mu);
+      else s4d_walk_fwd<1>(ds, gs, cs, cn, lane, A2_0, W, P, mu);
+      j = e;
+      e = e2;
+      if (j == L) {  // exact: the final-state gradient, decayed through every step after t1 - 1
+        if (dfrow && act) {
+          powers<8>(ex2(W), P);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mu[k] = fma2(P[k], make_float2(dfrow[2 * k], dfrow[2 * k + 1]), mu[k]);
+        }
+        break;
+      }
+      const int l2 = live_pairs(warp_max_f(act ? ex2(W) : 0.0f));
+      if (l2 == 0) break;
+      live = l2 < live ? l2 : live;
+    }
+  }
+
+  // ---- 4. chunks backwards ----------------------------------------------------------------------------
+  float2 dA[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) dA[k] = make_float2(0.0f, 0.0f);
+  const int64_t ck0 = t0 / kChunk, ck1 = (t1 - 1) / kChunk;
+  auto span = [&](int64_t ck, int64_t& s, int64_t& e) {
+    s = ck * kChunk > t0 ? ck * kChunk : t0;
+    e = (ck + 1) * kChunk < t1 ? (ck + 1) * kChunk : t1;
+  };
+  // the saved state entering chunk ck (> ck0): the end state of chunk ck - 1
+  auto ws_load = [&](int64_t ck, float2 (&hn)[8]) {
+    const float* w = p.ws + ((b * p.nck + ck - 1) * 16) * D + d;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      hn[k] = act ? make_float2(w[static_cast<int64_t>(2 * k) * D], w[static_cast<int64_t>(2 * k + 1) * D])
+                  : make_float2(0.0f, 0.0f);
+  };
+  float2 hn[8];
+  {
+    int64_t s, e;
+    span(ck1, s, e);
+    chunk_load<T, true, true, true, true>(p, b, d, act, lane, s, static_cast<int>(e - s), nx);
+    if (ck1 > ck0) ws_load(ck1, hn);
+  }
+  const int sw = lane & 7;
+  for (int64_t ck = ck1; ck >= ck0; --ck) {
+    int64_t s, e;
+    span(ck, s, e);
+    const int cn = static_cast<int>(e - s);
+    chunk_store<true, true, true, true>(nx, lane, xs, ds, gs, bs, cs);
+    if (ck > ck0) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) h[k] = hn[k];
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) h[k] = hst[k * 32 + lane];
+    }
+    if (ck > ck0) {  // the previous chunk's inputs and entering state, in flight during this chunk
+      int64_t s2, e2;
+      span(ck - 1, s2, e2);
+      chunk_load<T, true, true, true, true>(p, b, d, act, lane, s2, static_cast<int>(e2 - s2), nx);
+      if (ck - 1 > ck0) ws_load(ck - 1, hn);
+    }
+    // recompute the chunk's states: hs row i = the state before step i
+#pragma unroll 1
+    for (int i = 0; i < cn; ++i) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) hs[(i * 8 + k) * 32 + lane] = h[k];
+      s4d_fwd_step<ZOH>(xs[i * 32 + lane], ds[i * 32 + lane], bs + i * 16, A2_0, invA0, h);
+    }
+    // h now holds the state after the chunk's last step
+#pragma unroll 1
+    for (int i = cn - 1; i >= 0; --i) {
+      const int64_t t = s + i;
+      const float xv = xs[i * 32 + lane], dv = ds[i * 32 + lane], g = gs[i * 32 + lane];
+      const float2* brow = reinterpret_cast<const float2*>(bs + i * 16);
+      const float2* crow = reinterpret_cast<const float2*>(cs + i * 16);
+      float2 e[8];
+      step_e16(dv * A2_0, e);
+      const float2 gg = bc(g), dd = bc(dv);
+      float2 gd = make_float2(0.0f, 0.0f);  // sum_n (n + 1) lambda_n u_n (times A_0 below)
+      float2 sg = make_float2(0.0f, 0.0f);  // sum_n lambda_n B_n
+      float2 se = make_float2(0.0f, 0.0f);  // ZOH: sum_n lambda_n e_n B_n
+      float2 sq = make_float2(0.0f, 0.0f);  // ZOH: sum_n lambda_n e_n B_n / (n + 1)
+      float2 v[16];                         // this lane's dB terms (pairs 0..7) and dC terms (pairs 8..15)
+      const float2 dxv = bc(dv * xv), xq = bc(xv * invA0);
+      const float2 zq = bc(xv * dv * dv);   // ZOH: x delta^2
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 hp = hs[(i * 8 + k) * 32 + lane];  // h_{t-1}
+        const float2 lam = fma2(crow[k], gg, mu[k]);
+        const float2 lu = mul2(lam, fma2(e[k], hp, hp));  // lambda Abar h_{t-1}
+        dA[k] = fma2(lu, dd, dA[k]);
+        gd = fma2(lu, kPairN1[k], gd);
+        sg = fma2(lam, brow[k], sg);
+        v[8 + k] = mul2(gg, h[k]);  // dC: dy h_t
+        if (ZOH) {
+          const float2 le = mul2(lam, e[k]);
+          se = fma2(le, brow[k], se);
+          sq = fma2(le, mul2(brow[k], kPairInvN1[k]), sq);
+          v[k] = mul2(le, mul2(xq, kPairInvN1[k]));  // dB: lambda x e_n / A_n
+          const float2 w = mul2(kPairN1[k], bc(dv * A0));
+          dA[k] = fma2(mul2(mul2(lam, brow[k]), zq), zoh_f2(w, add2(e[k], bc(1.0f)), e[k]), dA[k]);
+        } else {
+          v[k] = mul2(lam, dxv);  // dB: lambda delta x
+        }
+        mu[k] = fma2(e[k], lam, lam);
+        h[k] = hp;
+      }
+      const float sgs = sg.x + sg.y;
+      float gx, gdt;
+      if (ZOH) {
+        gx = (sq.x + sq.y) * invA0;
+        gdt = fmaf(gd.x + gd.y, A0, xv * (sgs + se.x + se.y));
+      } else {
+        gx = dv * sgs;
+        gdt = fmaf(gd.x + gd.y, A0, xv * sgs);
+      }
+      if (act) {
+        const int64_t xi = (b * L + t) * D + d;
+        Elem<T>::store(p.dx, xi, gx);
+        Elem<T>::store(p.ddelta, xi, gdt);
+      }
+      // dB, dC: lane l writes its 32 terms as row l of the tile (16-byte pieces XOR-swizzled by l mod 8), then
+      // sums column l (term l of every lane)
+      float4* rrow = reinterpret_cast<float4*>(red + lane * 32);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) rrow[q ^ sw] = make_float4(v[2 * q].x, v[2 * q].y, v[2 * q + 1].x, v[2 * q + 1].y);
+      __syncwarp();
+      float2 acc[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int r = 0; r < 32; r += 2) {
+        const int c0 = (((lane >> 2) ^ (r & 7)) << 2) | (lane & 3);
+        const int c1 = (((lane >> 2) ^ ((r + 1) & 7)) << 2) | (lane & 3);
+        acc[(r >> 1) & 3] = add2(acc[(r >> 1) & 3], make_float2(red[r * 32 + c0], red[(r + 1) * 32 + c1]));
+      }
+      __syncwarp();
+      const float2 a01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+      atomicAdd((lane < 16 ? p.dB : p.dC) + (b * L + t) * 16 + (lane & 15), a01.x + a01.y);
+    }
+  }
+  if (act) {
+    if (t0 == 0 && p.dh0) {
+      float* out = p.dh0 + (b * D + d) * 16;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        out[2 * k] = mu[k].x;
+        out[2 * k + 1] = mu[k].y;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {  // dA_log_n = dA_n A_n, A_n = (n + 1) A_0
+      const float2 g = mul2(dA[k], mul2(kPairN1[k], bc(A0)));
+      atomicAdd(p.dA_log + d * 16 + 2 * k, g.x);
+      atomicAdd(p.dA_log + d * 16 + 2 * k + 1, g.y);
+    }
+  }
+}
+
+// floats of shared memory per warp: the generic layout, or the structured one where N = 16 may take it
+template <int NP>
+constexpr int kBwdSmemFloats = NP == 16 && kS4dWarpFloats > kBwdWarpFloats<NP> ? kS4dWarpFloats : kBwdWarpFloats<NP>;
+
 template <int NP, bool ZOH, typename T>
 __global__ void __launch_bounds__(kBwdWarps * 32, 1) scan_bwd_kernel(BwdParams p) {
   extern __shared__ float smem_bwd[];
@@ -403,7 +837,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) scan_bwd_kernel(BwdParams p
   if (gw >= p.nwarps) return;  // whole warp leaves together
   // this warp's shared memory: rows of states hs[(r * NP + n) * 32 + lane] (r = 0 the chunk's initial state,
   // r = 1 + i after step i of the chunk, r = kChunk + 1 the piece's initial state), then the staged chunk
-  float* hs = smem_bwd + static_cast<size_t>(wid) * kBwdWarpFloats<NP>;
+  float* hs = smem_bwd + static_cast<size_t>(wid) * kBwdSmemFloats<NP>;
   float* xs = hs + (kChunk + 2) * NP * 32;
   float* ds = xs + kChunk * 32;
   float* gs = ds + kChunk * 32;
@@ -442,7 +876,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) scan_bwd_kernel(BwdParams p
     }
     if constexpr (NP == 16) {
       if (__all_sync(0xffffffffu, s4d)) {
-        bwd_piece<NP, ZOH, T, true>(p, c, hs, xs, ds, gs, bs, cs, lane, row, t0, t1);
+        bwd_piece_s4d<ZOH, T>(p, act ? -expf(__ldg(p.A_log + d * N)) : -1.0f, hs, lane, row, t0, t1);
         continue;
       }
     }
@@ -452,7 +886,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) scan_bwd_kernel(BwdParams p
 
 template <int NP, bool ZOH, typename T>
 cudaError_t launch_bwd_np(const BwdParams& bp, cudaStream_t s) {
-  const size_t smem = static_cast<size_t>(kBwdWarps) * kBwdWarpFloats<NP> * sizeof(float);
+  const size_t smem = static_cast<size_t>(kBwdWarps) * kBwdSmemFloats<NP> * sizeof(float);
   auto kern = scan_bwd_kernel<NP, ZOH, T>;
   static bool attr_set[64] = {false};  // per device, once per instantiation
   int dev = 0;
