@@ -85,5 +85,7 @@ def test_compulsory_byte_and_flop_counts():
     ssd = dict(batch=1, L=64, H=2, P=16, N=64)
     # x, y: 2 * 2048 * 2; B, C: 2 * 4096 * 2; delta 128 * 4; A_log 2 * 4; final state 2048 * 4
     assert bench.ssd_bytes(ssd) == 8192 + 16384 + 512 + 8 + 8192
-    # one chunk per head: 2 Q^2 N + 2 Q^2 P + 4 Q N P with Q = 64
-    assert bench.ssd_flops(ssd) == 2 * (2 * 64 * 64 * 64 + 2 * 64 * 64 * 16 + 4 * 64 * 64 * 16)
+    # one chunk of Q = 128 steps (full tiles): C B^T once, 2 Q^2 N; per head 2 Q^2 P + 4 Q N P
+    assert bench.ssd_flops(ssd) == 2 * 128 * 128 * 64 + 2 * (2 * 128 * 128 * 16 + 4 * 128 * 64 * 16)
+    # one chunk of Q = 64 (the warp-MMA kernel's chunk length)
+    assert bench.ssd_flops(ssd, Q=64) == 2 * 64 * 64 * 64 + 2 * (2 * 64 * 64 * 16 + 4 * 64 * 64 * 16)
