@@ -699,14 +699,20 @@ def main(argv=None):
     value = job_value(units_step, K, world, total_s)
 
     # ---- end to end through the public API: pinned host inputs in, results back to the host ------------
+    # The prefill goes through ssm_scan_fwd_host (host arrays, streamed through the device in segments whose
+    # uploads, scan and downloads overlap); the decode step then copies the final state and the token in,
+    # steps on the device and copies y_t out.
     e2e = None
     if not args.no_e2e:
         hy = torch.empty((b, L, D), dtype=tdt).pin_memory()
         hs = torch.empty((b, D, N), dtype=torch.float32).pin_memory()
         hyt = torch.empty((b, D), dtype=tdt).pin_memory()
+        seg = min(lib.HOST_SEGMENT_STEPS, L)
+        hws = torch.empty(lib.host_workspace_size(b, D, N, cfg["dtype"], seg), dtype=torch.uint8, device="cuda")
         KE = max(3, min(K, 200))
         eve = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(KE)]
-        h2d = sum(t.numel() * t.element_size() for t in list(hx.values()) + list(ht.values()))
+        h2d = sum(t.numel() * t.element_size() for t in list(hx.values()) + list(ht.values())) + \
+            hs.numel() * hs.element_size()
         d2h = sum(t.numel() * t.element_size() for t in (hy, hs, hyt))
         if world > 1:
             dist.barrier()
@@ -714,20 +720,20 @@ def main(argv=None):
         for i in range(KE):
             flush.zero_()
             eve[i][0].record(stream)
-            for k in hx:
-                dev[k].copy_(hx[k], non_blocking=True)
+            lib.ssm_scan_fwd_host(hx["x"], hx["delta"], hx["A_log"], hx["B"], hx["C"], disc=cfg["disc"], y=hy,
+                                  final_state=hs, workspace=hws, stream=stream, seg_L=seg)
+            state.copy_(hs, non_blocking=True)
             for k in ht:
                 dtok[k].copy_(ht[k], non_blocking=True)
-            fwd()
             step()
-            hy.copy_(y, non_blocking=True)
-            hs.copy_(state, non_blocking=True)
             hyt.copy_(y_t, non_blocking=True)
             eve[i][1].record(stream)
         torch.cuda.synchronize()
+        lib.check_device()
         e2e_s = job_seconds(sum(e[0].elapsed_time(e[1]) for e in eve) / 1e3, world, device="cuda")
         e2e = {"value": job_value(units_step, KE, world, e2e_s), "unit": "elems/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": KE}
+               "d2h_bytes_per_step": d2h, "steps": KE, "segment_steps": seg,
+               "path": "ssm_scan_fwd_host (segments streamed from pinned host memory) + ssm_scan_step"}
 
     if rank != 0:
         if world > 1:

@@ -114,6 +114,36 @@ ssm_status ssm_scan_fwd_ex(const void *x, const void *delta, const float *A_log,
                            ssm_dtype dtype, ssm_disc disc, void *stream);
 
 /*
+ * Prefill of ssm_scan_fwd with every data array in HOST memory: x, delta, B, C, y and final_state (and A_log,
+ * h0) are host pointers, in the layouts of ssm_scan_fwd. The sequence is streamed through the device in
+ * segments of seg_L steps: segment k + 1 is copied in while segment k is computed and segment k - 1's y is
+ * copied out. Segments chain exactly through the state (h0 of segment k = final state of segment k - 1;
+ * "Understanding Mamba" s3.2: the recurrence carries everything about the past in h), so y and final_state
+ * are those of one ssm_scan_fwd over the whole sequence, computed by the same kernels. No counterpart in the
+ * pages: a way to feed the path from host memory without a full-size device copy.
+ *  - workspace: DEVICE memory of at least ssm_scan_fwd_host_workspace_size(batch, D, N, dtype, seg_L) bytes,
+ *    owned by the caller: two segment slots (x, delta, B, C, y), two states and A_log. Too small, or seg_L < 1:
+ *    SSM_ERR_INVALID_ARG.
+ *  - Copies use cudaMemcpyAsync / cudaMemcpy2DAsync; they overlap compute only when the host arrays are
+ *    page-locked (cudaHostAlloc / cudaHostRegister). Host arrays must stay valid, and untouched by the caller,
+ *    until `stream` has completed the call's work.
+ *  - Ordering: every copy and kernel is ordered after the work already on `stream` and before the work
+ *    enqueued on it afterwards. Internally the uploads and downloads run on two library-owned streams per
+ *    device (created on first use, kept for the life of the process) joined to `stream` by events; concurrent
+ *    calls on one device are serialised while they are enqueued.
+ *  - L = 0: final_state is set to h0 (or zeros) on the host before the call returns.
+ *  - Errors: argument errors as for ssm_scan_fwd (host ranges of outputs may not overlap inputs), CUDA
+ *    errors as SSM_ERR_CUDA; kernel-side failures are reported by ssm_check_device(stream).
+ */
+size_t ssm_scan_fwd_host_workspace_size(int64_t batch, int64_t D, int64_t N, ssm_dtype dtype, int64_t seg_L);
+ssm_status ssm_scan_fwd_host(const void *x, const void *delta, const float *A_log,
+                             const void *B, const void *C, const float *h0,
+                             void *y, float *final_state,
+                             void *workspace, size_t workspace_bytes, int64_t seg_L,
+                             int64_t batch, int64_t L, int64_t D, int64_t N,
+                             ssm_dtype dtype, ssm_disc disc, void *stream);
+
+/*
  * One decode step with the same optional pieces (z_t [batch, D] in `dtype`): the step of ssm_scan_step on
  * delta = softplus(delta_t + delta_bias[d]) (or delta_t + delta_bias[d]), output
  * y_t = (C_t . h + D_skip[d] x_t) * SiLU(z_t).

@@ -20,7 +20,8 @@ from __future__ import annotations
 from . import _ffi
 from ._ffi import SsmError
 
-__all__ = ["ssm_scan_fwd", "ssm_scan_step", "ssm_scan_bwd", "ssm_scan_fwd_ptr", "ssm_scan_step_ptr",
+__all__ = ["ssm_scan_fwd", "ssm_scan_fwd_host", "host_workspace_size", "ssm_scan_step", "ssm_scan_bwd",
+           "ssm_scan_fwd_ptr", "ssm_scan_step_ptr",
            "bwd_workspace_size", "ssm_ssd_fwd", "ssd_workspace_size", "check_device", "set_wait_limit_ns", "SsmError",
            "version"]
 
@@ -94,6 +95,9 @@ def ssm_scan_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, y=None,
                  D_skip=None, z=None):
     """Prefill selective scan. Returns (y, final_state) (final_state None if not wanted)."""
     torch = _torch()
+    if x.device.type == "cpu" and delta_bias is None and D_skip is None and z is None and not delta_softplus:
+        return ssm_scan_fwd_host(x, delta, A_log, B, C, disc, h0, y=y, final_state=final_state,
+                                 want_final_state=want_final_state, stream=stream)
     if x.device.type == "cpu":
         dev = torch.device("cuda", torch.cuda.current_device())
         xd, dd, ad, bd, cd, hd, bb, ds, zd = _to_device([x, delta, A_log, B, C, h0, delta_bias, D_skip, z], dev)
@@ -126,6 +130,54 @@ def ssm_scan_fwd(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, y=None,
                                      _ptr(final_state), batch, L, D, N, code, _ffi.DISC[disc],
                                      ctypes_void(s.cuda_stream))
     _ffi.check("ssm_scan_fwd", st)
+    return y, final_state
+
+
+HOST_SEGMENT_STEPS = 8192  # default segment of ssm_scan_fwd_host: about 100 MB of fp32 uploads at D = 1536
+
+
+def host_workspace_size(batch, D, N, dtype="f32", seg_L=HOST_SEGMENT_STEPS):
+    """Bytes of device workspace ssm_scan_fwd_host needs (0 for invalid sizes)."""
+    return int(_ffi.load().ssm_scan_fwd_host_workspace_size(batch, D, N, _ffi.DTYPE[dtype], seg_L))
+
+
+def ssm_scan_fwd_host(x, delta, A_log, B, C, disc: str = "euler", h0=None, *, y=None, final_state=None,
+                      want_final_state: bool = True, stream=None, seg_L: int = HOST_SEGMENT_STEPS, workspace=None):
+    """Prefill on HOST tensors (x, delta, B, C, A_log, h0, and the outputs y, final_state on the CPU), streamed
+    through the device segment by segment by ssm_scan_fwd_host: uploads, the scan and downloads overlap when
+    the host tensors are pinned. ``workspace``: a device uint8 tensor of host_workspace_size(...) bytes, or
+    None to allocate one here. Waits for the stream before returning, so the host outputs are complete."""
+    torch = _torch()
+    batch, L, D = x.shape
+    N = A_log.shape[-1]
+    code = _dtype_code(x)
+    dname = "bf16" if code == _ffi.DTYPE["bf16"] else "f32"
+    for name, t in (("delta", delta), ("B", B), ("C", C)):
+        if t.dtype != x.dtype:
+            raise TypeError(f"{name} has dtype {t.dtype}, x has {x.dtype}")
+    if A_log.dtype != torch.float32 or (h0 is not None and h0.dtype != torch.float32):
+        raise TypeError("A_log and h0 must be float32")
+    if tuple(delta.shape) != (batch, L, D) or tuple(B.shape) != (batch, L, N) or tuple(C.shape) != (batch, L, N) \
+            or tuple(A_log.shape) != (D, N) or (h0 is not None and tuple(h0.shape) != (batch, D, N)):
+        raise ValueError("shape mismatch: x/delta [b,L,D], B/C [b,L,N], A_log [D,N], h0 [b,D,N]")
+    ts = [x, delta, A_log, B, C] + ([h0] if h0 is not None else [])
+    if any(t.device.type != "cpu" or not t.is_contiguous() for t in ts):
+        raise ValueError("ssm_scan_fwd_host: inputs must be contiguous CPU tensors")
+    if y is None:
+        y = torch.empty((batch, L, D), dtype=x.dtype, pin_memory=True)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((batch, D, N), dtype=torch.float32, pin_memory=True)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    seg_L = max(1, min(int(seg_L), max(L, 1)))
+    need = host_workspace_size(batch, D, N, dname, seg_L)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    st = _ffi.load().ssm_scan_fwd_host(_ptr(x), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(h0), _ptr(y),
+                                       _ptr(final_state), _ptr(workspace), workspace.numel(), seg_L, batch, L, D,
+                                       N, code, _ffi.DISC[disc], ctypes_void(s.cuda_stream))
+    _ffi.check("ssm_scan_fwd_host", st)
+    s.synchronize()
     return y, final_state
 
 

@@ -19,6 +19,9 @@ _vp, _i64, _i32, _fp = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_v
 SIGNATURES = {
     "ssm_scan_fwd": (_i32, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i64, _i64, _i64, _i64, _i32, _i32, _vp]),
     "ssm_scan_step": (_i32, [_fp, _vp, _vp, _fp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _i32, _vp]),
+    "ssm_scan_fwd_host": (_i32, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _vp, ctypes.c_size_t, _i64, _i64, _i64, _i64,
+                                 _i64, _i32, _i32, _vp]),
+    "ssm_scan_fwd_host_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i64]),
     "ssm_scan_fwd_ex": (_i32, [_vp, _vp, _fp, _vp, _vp, _fp, _fp, _i32, _fp, _vp, _vp, _fp, _i64, _i64, _i64, _i64,
                                _i32, _i32, _vp]),
     "ssm_scan_step_ex": (_i32, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _i32, _fp, _vp, _vp, _i64, _i64, _i64, _i32, _i32,

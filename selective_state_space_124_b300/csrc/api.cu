@@ -7,6 +7,7 @@
 #include "launch.h"
 
 #include <atomic>
+#include <mutex>
 
 namespace ssm {
 
@@ -61,6 +62,66 @@ int sm_count() {
   return cached[dev];
 }
 
+namespace {
+// Library-owned copy streams and events of ssm_scan_fwd_host, one set per device, created on first use.
+struct HostStreamSet {
+  std::mutex mu;  // held while a call enqueues its work
+  bool ready = false;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t start, fin, ev_up[2], ev_comp[2], ev_down[2];
+};
+HostStreamSet g_host_sets[64];
+
+cudaError_t host_set_init(HostStreamSet& h) {
+  if (h.ready) return cudaSuccess;
+  cudaError_t e;
+  if ((e = cudaStreamCreateWithFlags(&h.up, cudaStreamNonBlocking)) != cudaSuccess) return e;
+  if ((e = cudaStreamCreateWithFlags(&h.down, cudaStreamNonBlocking)) != cudaSuccess) return e;
+  cudaEvent_t* evs[] = {&h.start, &h.fin, &h.ev_up[0], &h.ev_up[1], &h.ev_comp[0], &h.ev_comp[1],
+                        &h.ev_down[0], &h.ev_down[1]};
+  for (cudaEvent_t* ev : evs)
+    if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+  h.ready = true;
+  return cudaSuccess;
+}
+
+// Workspace of ssm_scan_fwd_host: A_log, two states, then two slots of (x, delta, B, C, y) for seg_L steps,
+// every piece 256-byte aligned.
+struct HostLayout {
+  size_t a_log, st[2], x[2], d[2], b[2], c[2], y[2], bytes;
+};
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+HostLayout host_layout(int64_t batch, int64_t D, int64_t N, int64_t es, int64_t seg_L) {
+  HostLayout l;
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    const size_t at = off;
+    off += align256(n);
+    return at;
+  };
+  const size_t sd = static_cast<size_t>(batch) * seg_L * D * es, sn = static_cast<size_t>(batch) * seg_L * N * es;
+  l.a_log = take(static_cast<size_t>(D) * N * 4);
+  for (int k = 0; k < 2; ++k) l.st[k] = take(static_cast<size_t>(batch) * D * N * 4);
+  for (int k = 0; k < 2; ++k) {
+    l.x[k] = take(sd);
+    l.d[k] = take(sd);
+    l.b[k] = take(sn);
+    l.c[k] = take(sn);
+    l.y[k] = take(sd);
+  }
+  l.bytes = off;
+  return l;
+}
+
+// rows of `width` bytes: batch rows, `hpitch` apart on the host, packed on the device
+cudaError_t copy_rows(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, int64_t rows,
+                      cudaMemcpyKind kind, cudaStream_t s) {
+  if (width == 0 || rows == 0) return cudaSuccess;
+  if (rows == 1) return cudaMemcpyAsync(dst, src, width, kind, s);
+  return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, static_cast<size_t>(rows), kind, s);
+}
+}  // namespace
+
 }  // namespace ssm
 
 using namespace ssm;
@@ -110,6 +171,108 @@ ssm_status ssm_scan_fwd_ex(const void* x, const void* delta, const float* A_log,
   if (batch == 0 || D == 0) return SSM_OK;
   cudaError_t e = (L == 0) ? launch_init_state(a) : (tma_path_ok(a) ? launch_fwd_tma(a) : launch_fwd_simple(a));
   if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd launch");
+  return SSM_OK;
+}
+
+size_t ssm_scan_fwd_host_workspace_size(int64_t batch, int64_t D, int64_t N, ssm_dtype dtype, int64_t seg_L) {
+  if (batch < 0 || D < 0 || N < 1 || N > 16 || seg_L < 1 || !valid_enums(dtype, SSM_DISC_EULER)) return 0;
+  int64_t t;
+  if (!mul_ok(batch, seg_L, &t) || !mul_ok(t, D + N, &t) || !mul_ok(t, 64, &t)) return 0;
+  return host_layout(batch, D, N, dtype == SSM_DTYPE_BF16 ? 2 : 4, seg_L).bytes;
+}
+
+ssm_status ssm_scan_fwd_host(const void* x, const void* delta, const float* A_log, const void* B, const void* C,
+                             const float* h0, void* y, float* final_state, void* workspace, size_t workspace_bytes,
+                             int64_t seg_L, int64_t batch, int64_t L, int64_t D, int64_t N, ssm_dtype dtype,
+                             ssm_disc disc, void* stream) {
+  g_last_error[0] = '\0';
+  if (!valid_enums(dtype, disc)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: bad dtype or disc");
+  if (batch < 0 || L < 0 || D < 0 || N < 1)
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: sizes must be >= 0 and N >= 1");
+  if (N > 16) return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd_host: N = %lld > 16", (long long)N);
+  if (seg_L < 1) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: seg_L must be >= 1");
+  int64_t bl, bld, bln, bd, bdn, tmp;
+  if (!mul_ok(batch, L, &bl) || !mul_ok(bl, D, &bld) || !mul_ok(bl, N, &bln) || !mul_ok(batch, D, &bd) ||
+      !mul_ok(bd, N, &bdn) || !mul_ok(batch, seg_L, &tmp) || !mul_ok(tmp, D + N, &tmp) || !mul_ok(tmp, 64, &tmp))
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: sizes overflow");
+  const int64_t es = dtype == SSM_DTYPE_BF16 ? 2 : 4;
+  if (bld > 0 && (!x || !delta || !y)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: null x/delta/y");
+  if (bln > 0 && (!B || !C)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: null B/C");
+  if (bld > 0 && !A_log) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: null A_log");
+  const Range ry = range_of(y, bld, es);
+  const Range rf = range_of(final_state, final_state ? bdn : 0, 4);
+  const Range ins[] = {range_of(x, bld, es), range_of(delta, bld, es), range_of(A_log, D * N, 4),
+                       range_of(B, bln, es), range_of(C, bln, es),     range_of(h0, h0 ? bdn : 0, 4)};
+  for (const Range& r : ins)
+    if (overlap(ry, r) || overlap(rf, r))
+      return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: outputs overlap inputs");
+  if (overlap(ry, rf)) return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: y overlaps final_state");
+  if (batch == 0 || D == 0) return SSM_OK;
+  if (L == 0) {  // no steps: the final state is the initial one
+    if (final_state) {
+      if (h0) std::memcpy(final_state, h0, static_cast<size_t>(bdn) * 4);
+      else std::memset(final_state, 0, static_cast<size_t>(bdn) * 4);
+    }
+    return SSM_OK;
+  }
+  const HostLayout l = host_layout(batch, D, N, es, seg_L);
+  if (!workspace || workspace_bytes < l.bytes)
+    return fail(SSM_ERR_INVALID_ARG, "ssm_scan_fwd_host: workspace of %zu bytes, %zu needed", workspace_bytes, l.bytes);
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd_host");
+  if (dev < 0 || dev >= 64) return fail(SSM_ERR_UNSUPPORTED, "ssm_scan_fwd_host: device %d", dev);
+  HostStreamSet& hs = g_host_sets[dev];
+  std::lock_guard<std::mutex> lock(hs.mu);
+  if ((e = host_set_init(hs)) != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd_host: streams");
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  unsigned char* w = static_cast<unsigned char*>(workspace);
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+#define SSM_HOST_CK(expr)                                                      \
+  do {                                                                         \
+    if ((e = (expr)) != cudaSuccess) return cuda_fail(e, "ssm_scan_fwd_host"); \
+  } while (0)
+  // everything after the work already on the caller's stream
+  SSM_HOST_CK(cudaEventRecord(hs.start, cs));
+  SSM_HOST_CK(cudaStreamWaitEvent(hs.up, hs.start, 0));
+  SSM_HOST_CK(cudaStreamWaitEvent(hs.down, hs.start, 0));
+  SSM_HOST_CK(cudaMemcpyAsync(w + l.a_log, A_log, static_cast<size_t>(D) * N * 4, h2d, hs.up));
+  if (h0) SSM_HOST_CK(cudaMemcpyAsync(w + l.st[1], h0, static_cast<size_t>(bdn) * 4, h2d, hs.up));
+  const int64_t nseg = (L + seg_L - 1) / seg_L;
+  const size_t hrow_d = static_cast<size_t>(L) * D * es, hrow_n = static_cast<size_t>(L) * N * es;
+  for (int64_t sg = 0; sg < nseg; ++sg) {
+    const int k = static_cast<int>(sg & 1);
+    const int64_t t0 = sg * seg_L, n = seg_L < L - t0 ? seg_L : L - t0;
+    const size_t wd = static_cast<size_t>(n) * D * es, wn = static_cast<size_t>(n) * N * es;
+    const size_t od = static_cast<size_t>(t0) * D * es, on = static_cast<size_t>(t0) * N * es;
+    // slot k's inputs are free once the compute of segment sg - 2 is done
+    if (sg >= 2) SSM_HOST_CK(cudaStreamWaitEvent(hs.up, hs.ev_comp[k], 0));
+    SSM_HOST_CK(copy_rows(w + l.x[k], wd, static_cast<const char*>(x) + od, hrow_d, wd, batch, h2d, hs.up));
+    SSM_HOST_CK(copy_rows(w + l.d[k], wd, static_cast<const char*>(delta) + od, hrow_d, wd, batch, h2d, hs.up));
+    SSM_HOST_CK(copy_rows(w + l.b[k], wn, static_cast<const char*>(B) + on, hrow_n, wn, batch, h2d, hs.up));
+    SSM_HOST_CK(copy_rows(w + l.c[k], wn, static_cast<const char*>(C) + on, hrow_n, wn, batch, h2d, hs.up));
+    SSM_HOST_CK(cudaEventRecord(hs.ev_up[k], hs.up));
+    SSM_HOST_CK(cudaStreamWaitEvent(cs, hs.ev_up[k], 0));
+    // slot k's y is free once the copy-out of segment sg - 2 is done
+    if (sg >= 2) SSM_HOST_CK(cudaStreamWaitEvent(cs, hs.ev_down[k], 0));
+    const float* hin = sg == 0 ? (h0 ? reinterpret_cast<const float*>(w + l.st[1]) : nullptr)
+                               : reinterpret_cast<const float*>(w + l.st[(sg - 1) & 1]);
+    const ssm_status st = ssm_scan_fwd(w + l.x[k], w + l.d[k], reinterpret_cast<const float*>(w + l.a_log),
+                                       w + l.b[k], w + l.c[k], hin, w + l.y[k],
+                                       reinterpret_cast<float*>(w + l.st[k]), batch, n, D, N, dtype, disc, cs);
+    if (st != SSM_OK) return st;
+    SSM_HOST_CK(cudaEventRecord(hs.ev_comp[k], cs));
+    SSM_HOST_CK(cudaStreamWaitEvent(hs.down, hs.ev_comp[k], 0));
+    SSM_HOST_CK(copy_rows(static_cast<char*>(y) + od, hrow_d, w + l.y[k], wd, wd, batch, d2h, hs.down));
+    SSM_HOST_CK(cudaEventRecord(hs.ev_down[k], hs.down));
+  }
+  if (final_state)
+    SSM_HOST_CK(cudaMemcpyAsync(final_state, w + l.st[(nseg - 1) & 1], static_cast<size_t>(bdn) * 4, d2h, hs.down));
+  // the caller's stream continues after the last copy-out (the last upload precedes the last compute)
+  SSM_HOST_CK(cudaEventRecord(hs.fin, hs.down));
+  SSM_HOST_CK(cudaStreamWaitEvent(cs, hs.fin, 0));
+#undef SSM_HOST_CK
   return SSM_OK;
 }
 

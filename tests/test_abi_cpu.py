@@ -170,3 +170,49 @@ def test_wait_limit_round_trip(lib):
         assert lib.ssm_set_wait_limit_ns(456) == 123
     finally:
         assert lib.ssm_set_wait_limit_ns(prev) == 456
+
+
+def fwd_host(lib, *, x=FAKE, delta=FAKE + (1 << 30), A_log=FAKE + (2 << 30), B=FAKE + (3 << 30),
+             C=FAKE + (4 << 30), h0=None, y=FAKE + (5 << 30), fs=FAKE + (6 << 30), ws=FAKE + (7 << 30),
+             ws_bytes=1 << 20, seg_L=4, batch=1, L=8, D=4, N=16, dtype=0, disc=0):
+    v = lambda p: None if p is None else ctypes.c_void_p(p)
+    return lib.ssm_scan_fwd_host(v(x), v(delta), v(A_log), v(B), v(C), v(h0), v(y), v(fs), v(ws), ws_bytes, seg_L,
+                                 batch, L, D, N, dtype, disc, None)
+
+
+def test_fwd_host_argument_errors(lib):
+    """The host-streaming prefill checks its arguments before any copy: sizes, pointers, segment length,
+    output ranges and the workspace size."""
+    assert fwd_host(lib, seg_L=0) == _ffi.SSM_ERR_INVALID_ARG
+    assert b"seg_L" in lib.ssm_last_error()
+    assert fwd_host(lib, N=17) == _ffi.SSM_ERR_UNSUPPORTED
+    assert fwd_host(lib, x=None) == _ffi.SSM_ERR_INVALID_ARG
+    assert fwd_host(lib, y=FAKE + 8) == _ffi.SSM_ERR_INVALID_ARG  # y overlaps x
+    need = lib.ssm_scan_fwd_host_workspace_size(1, 4, 16, 0, 4)
+    assert fwd_host(lib, ws_bytes=need - 1) == _ffi.SSM_ERR_INVALID_ARG
+    assert b"needed" in lib.ssm_last_error()
+    assert fwd_host(lib, ws=None) == _ffi.SSM_ERR_INVALID_ARG
+
+
+def test_fwd_host_workspace_size(lib):
+    """Two segment slots of x, delta, B, C and y, two states and A_log, each piece 256-byte aligned."""
+    up = lambda v: (v + 255) // 256 * 256
+    for batch, D, N, dtype, seg in [(1, 1536, 16, 0, 8192), (2, 100, 4, 1, 37), (3, 5, 1, 0, 1)]:
+        es = 2 if dtype == 1 else 4
+        sd, sn = batch * seg * D * es, batch * seg * N * es
+        want = up(D * N * 4) + 2 * up(batch * D * N * 4) + 2 * (3 * up(sd) + 2 * up(sn))
+        assert lib.ssm_scan_fwd_host_workspace_size(batch, D, N, dtype, seg) == want
+    assert lib.ssm_scan_fwd_host_workspace_size(1, 4, 16, 0, 0) == 0
+    assert lib.ssm_scan_fwd_host_workspace_size(1, 4, 17, 0, 8) == 0
+
+
+def test_fwd_host_no_steps_copies_the_initial_state(lib):
+    """L = 0: the final state is h0 (or zeros), written on the host, with no device work."""
+    import numpy as np
+    h0 = np.arange(2 * 3 * 4, dtype=np.float32).reshape(2, 3, 4) - 5.0
+    fs = np.full_like(h0, 7.0)
+    p = lambda a: a.ctypes.data
+    assert fwd_host(lib, h0=p(h0), fs=p(fs), batch=2, L=0, D=3, N=4, ws=None, ws_bytes=0) == _ffi.SSM_OK
+    assert np.array_equal(fs, h0)
+    assert fwd_host(lib, h0=None, fs=p(fs), batch=2, L=0, D=3, N=4, ws=None, ws_bytes=0) == _ffi.SSM_OK
+    assert not fs.any()
