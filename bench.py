@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=None,
                     help="CPU oracle seconds per sample (default: 5 for the GPU arm's baseline, "
                          "120 / (steps + warmup) for --impl reference)")
+    ap.add_argument("--oracle-threads", type=int, default=None,
+                    help="threads of the CPU oracle in --impl reference (default: every host core)")
     ap.add_argument("--set", action="append", default=[], metavar="KEY=VALUE",
                     help="override a size of the workload (batch, L or D), e.g. for a small profiling case")
     ap.add_argument("--no-extra", action="store_true",
@@ -506,10 +508,10 @@ def oracle_threads() -> int:
         return os.cpu_count() or 1
 
 
-def pin_oracle_threads() -> None:
-    """Fix the oracle's OpenMP thread count before its library (and so libgomp) is loaded, so that both
-    bench arms time it on the same number of threads."""
-    os.environ["OMP_NUM_THREADS"] = str(oracle_threads())
+def pin_oracle_threads(n=None) -> None:
+    """Fix the oracle's OpenMP thread count (default: every host core) before its library (and so libgomp) is
+    loaded, so that both bench arms time it on the same number of threads."""
+    os.environ["OMP_NUM_THREADS"] = str(n if n else oracle_threads())
 
 
 def oracle_sample(inp, cfg, budget_s):
@@ -560,7 +562,7 @@ def run_reference(args, rank):
     """The reference arm: the CPU oracle as it stands, on the host cores, one bounded sample per step."""
     if rank != 0:
         return
-    pin_oracle_threads()
+    pin_oracle_threads(args.oracle_threads)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     overrides, cfg, config = workload_config(args, world)
     inp = ssm_inputs.workload_inputs(args.workload, **overrides)
@@ -587,23 +589,34 @@ def run_reference(args, rank):
 
 def cpu_baseline_subprocess(args):
     """The oracle timed in a fresh process (no torch, no CUDA context, OpenMP pinned to the host cores),
-    exactly as the reference arm times it: 1 untimed and 2 timed samples of the same workload."""
-    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", args.workload,
-           "--steps", "2", "--warmup", "1", "--cpu-seconds", str(args.cpu_seconds or 5.0)]
-    for kv in args.set:
-        cmd += ["--set", kv]
-    env = {k: v for k, v in os.environ.items()
-           if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "LOCAL_WORLD_SIZE", "GROUP_RANK", "ROLE_RANK",
-                        "TORCHELASTIC_RUN_ID", "MASTER_ADDR", "MASTER_PORT")}
-    env["OMP_NUM_THREADS"] = str(oracle_threads())
-    try:
+    exactly as the reference arm times it: 1 untimed and 2 timed samples of the same workload. A second,
+    shorter run on one thread gives the per-core rate."""
+    def run(threads, seconds):
+        cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", args.workload,
+               "--steps", "2", "--warmup", "1", "--cpu-seconds", str(seconds), "--oracle-threads", str(threads)]
+        for kv in args.set:
+            cmd += ["--set", kv]
+        env = {k: v for k, v in os.environ.items()
+               if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "LOCAL_WORLD_SIZE", "GROUP_RANK", "ROLE_RANK",
+                            "TORCHELASTIC_RUN_ID", "MASTER_ADDR", "MASTER_PORT")}
+        env["OMP_NUM_THREADS"] = str(threads)
         out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900, check=True).stdout
         rec = json.loads(out.strip().splitlines()[-1])["cpu_baseline"]
+        rec["sample"] = rec["sample"].replace("each step: ", "median of 2 timed samples, each ")
+        return rec
+
+    try:
+        rec = run(oracle_threads(), args.cpu_seconds or 5.0)
     except (subprocess.SubprocessError, ValueError, KeyError, IndexError) as e:
         return {"value": None, "unit": "elems/s", "cores": None, "kind": "oracle",
                 "sample": f"unavailable: {type(e).__name__}: {str(e)[:200]}"}
-    rec["sample"] = rec["sample"].replace("each step: ", "median of 2 timed samples, each ")
     rec["process"] = "separate process, OMP_NUM_THREADS = host cores (as the reference arm)"
+    try:
+        one = run(1, 1.0)
+        rec["single_thread"] = {"value": one["value"], "unit": "elems/s", "cores": one["cores"],
+                                "sample": one["sample"]}
+    except (subprocess.SubprocessError, ValueError, KeyError, IndexError) as e:
+        rec["single_thread"] = {"value": None, "sample": f"unavailable: {type(e).__name__}: {str(e)[:200]}"}
     return rec
 
 
