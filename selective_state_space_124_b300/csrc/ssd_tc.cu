@@ -57,6 +57,12 @@ __device__ __forceinline__ void mb_init(unsigned long long* b) {
 __device__ __forceinline__ void mb_expect(unsigned long long* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s32(b)), "r"(bytes) : "memory");
 }
+// Programmatic dependent launch: the next kernel of the layer may be scheduled from here on (its CTAs wait in
+// pdl_wait() until this grid has completed and its writes are visible); and the wait itself. Both are no-ops
+// for a kernel launched without the programmatic-serialisation attribute.
+__device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Bounded wait for phase `parity` of an mbarrier (every calling thread waits; no warp-wide agreement needed).
 __device__ __forceinline__ bool mb_wait(unsigned long long* b, uint32_t parity) {
   uint32_t ok = 0;
@@ -133,13 +139,6 @@ __device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  tmem_ld16_async(taddr, r);
-  tmem_wait();
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 __device__ __forceinline__ uint32_t bf2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -222,6 +221,7 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
   const int64_t npairs = (p.H + 1) / 2;
   const int64_t groups = (npairs + kPairsPerCta - 1) / kPairsPerCta;
   const int64_t g = blockIdx.x % groups, c = (blockIdx.x / groups) % p.nc, b = blockIdx.x / groups / p.nc;
+  pdl_allow_next();  // the state pass reads E and slast only after this grid completes (pdl_wait)
 
   if (tid == 0) {
     mb_init(&sm.barB);
@@ -356,6 +356,7 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
 // One thread per (b, h, p, 4 consecutive n).
 template <int N>
 __global__ void __launch_bounds__(256, 4) ssd_state_pass_kernel(TcParams p) {
+  pdl_wait();  // E and slast of launch 1
   const int64_t total = p.batch * p.H * kTP * (N / 4);
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= total) return;
@@ -459,6 +460,7 @@ __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__
       tma3(sm.BM + kb * kTQ * 128, &mB, kb * 64, static_cast<int>(c * kTQ), static_cast<int>(b), &sm.barCB);
     }
     pendCB = 0;
+    pdl_wait();  // S_c of launch 2 (the C and B tiles above are the layer's inputs)
     issue_xs(hbase, 0);
   }
   if (warp < nh) {  // warp w: decays of head hbase + w
@@ -706,10 +708,26 @@ cudaError_t launch_tc_n(const SsdArgs& a) {
   ssd_chunk_state_kernel<N, ZOH><<<static_cast<unsigned>(a.batch * p.nc * g1), kTT, smem1, a.stream>>>(mX, mB, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t threads = a.batch * a.H * kTP * (N / 4);
-  ssd_state_pass_kernel<N><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, a.stream>>>(p);
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg2 = {};
+  cfg2.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256));
+  cfg2.blockDim = dim3(256);
+  cfg2.stream = a.stream;
+  cfg2.attrs = pdl;
+  cfg2.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg2, ssd_state_pass_kernel<N>, p)) != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t g3 = (a.H + kHeadsPerCta - 1) / kHeadsPerCta;
-  ssd_output_kernel<N, ZOH><<<static_cast<unsigned>(a.batch * p.nc * g3), kTT, smem3, a.stream>>>(mX, mB, mC, mS, p);
+  cudaLaunchConfig_t cfg3 = {};
+  cfg3.gridDim = dim3(static_cast<unsigned>(a.batch * p.nc * g3));
+  cfg3.blockDim = dim3(kTT);
+  cfg3.dynamicSmemBytes = smem3;
+  cfg3.stream = a.stream;
+  cfg3.attrs = pdl;
+  cfg3.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg3, ssd_output_kernel<N, ZOH>, mX, mB, mC, mS, p)) != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
