@@ -309,6 +309,9 @@ __device__ __forceinline__ void bwd_piece(const BwdParams& p, const BwdChan<NP, 
   }
 
   // ---- 4. chunks backwards ----------------------------------------------------------------------------
+  // dB, dC and dA_log are zeroed by the launch before this kernel, which may still be running (programmatic
+  // dependent launch): wait for it before the first atomic add. A no-op once it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   float dA[NP];
 #pragma unroll
   for (int n = 0; n < NP; ++n) dA[n] = 0.0f;
@@ -684,6 +687,9 @@ __device__ __forceinline__ void bwd_piece_s4d(const BwdParams& p, float A0, floa
   }
 
   // ---- 4. chunks backwards ----------------------------------------------------------------------------
+  // dB, dC and dA_log are zeroed by the launch before this kernel, which may still be running (programmatic
+  // dependent launch): wait for it before the first atomic add. A no-op once it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   float2 dA[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) dA[k] = make_float2(0.0f, 0.0f);
@@ -898,7 +904,17 @@ cudaError_t launch_bwd_np(const BwdParams& bp, cudaStream_t s) {
     attr_set[dev & 63] = true;
   }
   const int64_t blocks = (bp.nwarps + kBwdWarps - 1) / kBwdWarps;
-  kern<<<static_cast<unsigned>(blocks), kBwdWarps * 32, smem, s>>>(bp);
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kBwdWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&cfg, kern, bp)) != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -907,6 +923,18 @@ cudaError_t launch_bwd_disc(const BwdParams& bp, cudaStream_t s) {
   if (bp.N <= 4) return launch_bwd_np<4, ZOH, T>(bp, s);
   if (bp.N <= 8) return launch_bwd_np<8, ZOH, T>(bp, s);
   return launch_bwd_np<16, ZOH, T>(bp, s);
+}
+
+// Zero dA_log, dB and dC (the atomic sums) in one launch; the backward kernel after it may start at once and
+// waits for this grid only before its first atomic add.
+__global__ void bwd_zero_kernel(float* a, int64_t na, float* b, int64_t nb, float* c, int64_t nc) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < na + nb + nc; i += stride) {
+    if (i < na) a[i] = 0.0f;
+    else if (i < na + nb) b[i - na] = 0.0f;
+    else c[i - na - nb] = 0.0f;
+  }
 }
 
 // dh0 = dfinal (or 0) when there are no steps.
@@ -954,12 +982,13 @@ size_t bwd_workspace_bytes(int64_t batch, int64_t L, int64_t D, int64_t N) {
 
 cudaError_t launch_bwd(const BwdArgs& a) {
   cudaError_t e = cudaSuccess;
-  const size_t da_bytes = static_cast<size_t>(a.D * a.N) * sizeof(float);
-  if (da_bytes && (e = cudaMemsetAsync(a.dA_log, 0, da_bytes, a.stream)) != cudaSuccess) return e;
-  const size_t bc_bytes = static_cast<size_t>(a.batch * a.L * a.N) * sizeof(float);
-  if (bc_bytes) {
-    if ((e = cudaMemsetAsync(a.dB, 0, bc_bytes, a.stream)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(a.dC, 0, bc_bytes, a.stream)) != cudaSuccess) return e;
+  const int64_t na = a.D * a.N, nbc = a.batch * a.L * a.N;
+  if (na + 2 * nbc > 0) {
+    const int64_t zb = (na + 2 * nbc + 255) / 256;
+    const int64_t zcap = static_cast<int64_t>(sm_count()) * 4;
+    bwd_zero_kernel<<<static_cast<unsigned>(zb < zcap ? zb : zcap), 256, 0, a.stream>>>(a.dA_log, na, a.dB, nbc,
+                                                                                          a.dC, nbc);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.L == 0) {
     const int64_t n = a.batch * a.D * a.N;
