@@ -23,9 +23,14 @@
 //   4. walks the chunks backwards: recomputes the chunk's states from its saved start into shared memory
 //      (each lane its own column, so no lane reads another's and no barrier is needed), then steps back
 //      through the chunk accumulating the gradients.
-// dB and dC sum over channels: each warp reduces its 32 lanes' terms with a shuffle reduce-scatter and adds
-// the result into the outputs with one atomic add per (step, entry) per warp; dA_log sums over the batch
-// and the time axis: one atomic add per entry per piece. The three are zeroed by the entry point first.
+// Two implementations of a piece: bwd_piece_s4d where every channel of the warp has the structured decay
+// A_n = (n + 1) A_0 at N = 16 (paired f32x2 arithmetic, one decay tree per step, pair-dropping walks), and
+// bwd_piece for any A and N <= 16.
+// dB and dC sum over channels: each warp reduces its 32 lanes' terms (a shared-memory transpose in the
+// structured path, a shuffle reduce-scatter in the generic one) and adds the result into the outputs with one
+// atomic add per (step, entry) per warp; dA_log sums over the batch and the time axis: one atomic add per
+// entry per piece. A zeroing kernel clears the three first; this kernel is launched as its programmatic
+// dependent and waits for it only before its first atomic add.
 #include <mutex>
 
 #include "common.cuh"
@@ -89,31 +94,14 @@ struct BwdChan {
   float invA[NP];  // 1 / A (ZOH), 0 where A == 0
 };
 
-// e_n = Abar_n - 1 of every entry at one step. Generic A: one SFU exp2 (and the cancellation-free series)
-// per entry. Structured A (A_n = (n + 1) A_0, checked per piece): one exp2 for entry 0, then the exact identity
-// e_{m+k+1} = e_m (1 + e_k) + e_k gives the others with one FMA each (a tree four levels deep).
-template <int NP, bool ZOH, bool S4D>
+// e_n = Abar_n - 1 of every entry at one step, for the generic path: one SFU exp2 (and the cancellation-free
+// series) per entry. (The structured path below derives all 16 from e_0 with the decay tree.)
+template <int NP, bool ZOH>
 __device__ __forceinline__ void step_e(const BwdChan<NP, ZOH>& c, float dt, float (&e)[NP]) {
-  if constexpr (S4D) {
-    static_assert(NP == 16, "the structured path covers N = 16");
-    const float w = dt * c.A2[0];
-    e[0] = exp2m1(w, ex2(w));
-    e[1] = fmaf(e[0], 1.0f + e[0], e[0]);
-    const float a1 = 1.0f + e[1];
-    e[2] = fmaf(e[0], a1, e[1]);
-    e[3] = fmaf(e[1], a1, e[1]);
-    const float a3 = 1.0f + e[3];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) e[4 + k] = fmaf(e[k], a3, e[3]);
-    const float a7 = 1.0f + e[7];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) e[8 + k] = fmaf(e[k], a7, e[7]);
-  } else {
-#pragma unroll
-    for (int n = 0; n < NP; ++n) {
-      const float w = dt * c.A2[n];
-      e[n] = exp2m1(w, ex2(w));
-    }
+  for (int n = 0; n < NP; ++n) {
+    const float w = dt * c.A2[n];
+    e[n] = exp2m1(w, ex2(w));
   }
 }
 
@@ -182,9 +170,8 @@ __device__ __forceinline__ void load_chunk(const BwdParams& p, int64_t b, int64_
   __syncwarp();
 }
 
-// One piece [t0, t1) of a row (see the file comment for the four phases). S4D selects the structured-A
-// decay tree at compile time.
-template <int NP, bool ZOH, typename T, bool S4D>
+// One piece [t0, t1) of a row, any A (see the file comment for the four phases).
+template <int NP, bool ZOH, typename T>
 __device__ __forceinline__ void bwd_piece(const BwdParams& p, const BwdChan<NP, ZOH>& c, float* hs, float* xs,
                                           float* ds, float* gs, float* bs, float* cs, int lane, int64_t row,
                                           int64_t t0, int64_t t1) {
@@ -212,7 +199,7 @@ __device__ __forceinline__ void bwd_piece(const BwdParams& p, const BwdChan<NP, 
       for (int i = cn - 1; i >= 0; --i) {
         const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
         float ev[NP];
-        step_e<NP, ZOH, S4D>(c, dt, ev);
+        step_e<NP, ZOH>(c, dt, ev);
 #pragma unroll
         for (int n = 0; n < NP; ++n) {
           h[n] = fmaf(P[n], bfac(c, n, dt, ev[n]) * bs[i * 16 + n] * xv, h[n]);
@@ -249,7 +236,7 @@ __device__ __forceinline__ void bwd_piece(const BwdParams& p, const BwdChan<NP, 
     for (int i = 0; i < cn; ++i) {
       const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
       float ev[NP];
-      step_e<NP, ZOH, S4D>(c, dt, ev);
+      step_e<NP, ZOH>(c, dt, ev);
 #pragma unroll
       for (int n = 0; n < NP; ++n) h[n] = fmaf(ev[n], h[n], h[n]) + bfac(c, n, dt, ev[n]) * bs[i * 16 + n] * xv;
     }
@@ -284,7 +271,7 @@ __device__ __forceinline__ void bwd_piece(const BwdParams& p, const BwdChan<NP, 
       for (int i = 0; i < cn; ++i) {
         const float dt = ds[i * 32 + lane], g = gs[i * 32 + lane];
         float ev[NP];
-        step_e<NP, ZOH, S4D>(c, dt, ev);
+        step_e<NP, ZOH>(c, dt, ev);
 #pragma unroll
         for (int n = 0; n < NP; ++n) {
           P[n] = fmaf(P[n], ev[n], P[n]);
@@ -334,7 +321,7 @@ __device__ __forceinline__ void bwd_piece(const BwdParams& p, const BwdChan<NP, 
     for (int i = 0; i < cn; ++i) {
       const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane];
       float ev[NP];
-      step_e<NP, ZOH, S4D>(c, dt, ev);
+      step_e<NP, ZOH>(c, dt, ev);
 #pragma unroll
       for (int n = 0; n < NP; ++n) {
         h[n] = fmaf(ev[n], h[n], h[n]) + bfac(c, n, dt, ev[n]) * bs[i * 16 + n] * xv;
@@ -347,7 +334,7 @@ __device__ __forceinline__ void bwd_piece(const BwdParams& p, const BwdChan<NP, 
       const float xv = xs[i * 32 + lane], dt = ds[i * 32 + lane], g = gs[i * 32 + lane];
       float gx = 0.0f, gdt = 0.0f;
       float ev[NP];
-      step_e<NP, ZOH, S4D>(c, dt, ev);
+      step_e<NP, ZOH>(c, dt, ev);
       float v[32];  // this lane's terms of dB (v[n]) and dC (v[16 + n]) at step t
 #pragma unroll
       for (int n = 0; n < 16; ++n) {
@@ -886,7 +873,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1) scan_bwd_kernel(BwdParams p
         continue;
       }
     }
-    bwd_piece<NP, ZOH, T, false>(p, c, hs, xs, ds, gs, bs, cs, lane, row, t0, t1);
+    bwd_piece<NP, ZOH, T>(p, c, hs, xs, ds, gs, bs, cs, lane, row, t0, t1);
   }
 }
 
