@@ -24,6 +24,8 @@
 // Steps past the sequence end read zeros (3-D tensor maps per batch element) and take delta = 0, so a last
 // partial chunk needs no special case. Every mbarrier wait is bounded (2 s); a wait that runs out sets this
 // file's status word, reported by ssm_check_device() as SSM_ERR_TIMEOUT.
+#include <cstddef>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -90,6 +92,17 @@ __device__ __forceinline__ void tma2(void* dst, const CUtensorMap* m, int c0, in
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(s32(dst)), "l"(m), "r"(c0), "r"(c1), "r"(s32(bar))
       : "memory");
+}
+// Bulk tensor store of a shared-memory box to global memory, tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void tma_store2(const CUtensorMap* m, int c0, int c1, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(m), "r"(c0), "r"(c1), "r"(s32(src))
+               : "memory");
+}
+// Commit the issued bulk stores and wait until they have read their shared-memory sources.
+__device__ __forceinline__ void tma_store_drain() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -214,7 +227,14 @@ struct ChunkSmem {
 
 template <int N, bool ZOH>
 __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_constant__ CUtensorMap mX,
-                                                              const __grid_constant__ CUtensorMap mB, TcParams p) {
+                                                              const __grid_constant__ CUtensorMap mB,
+                                                              const __grid_constant__ CUtensorMap mE, TcParams p) {
+  // E leaves through shared memory: the B and x tiles (contiguous, free once the MMA is done) hold the pair's
+  // [2 heads][N / 32 column blocks][64 rows][32 fp32] boxes, which bulk tensor stores write to the workspace.
+  // The B tile is loaded once per CTA, so this needs one head pair per CTA.
+  static_assert(kPairsPerCta == 1, "the E staging reuses the B tile");
+  static_assert(offsetof(ChunkSmem<N>, Xt) == N * 256 && N * 256 + 2 * kTQ * 128 >= 2 * kTP * N * 4,
+                "the B and x tiles must be contiguous and hold the pair's E");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   ChunkSmem<N>& sm = *reinterpret_cast<ChunkSmem<N>*>(smem_raw + ((1024u - (s32(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -315,25 +335,40 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
     if (!ok) break;
     if (tid == 0) pendM = -1;
     {
-      // row m of D is head h0 + m / 64, channel p = m % 64: write its N entries of E
+      // row m of D is head h0 + m / 64, channel p = m % 64: its N entries of E go to the staging boxes, rows of
+      // 128 bytes whose 16-byte pieces are XOR-swizzled by the row (the tensor map's 128-byte swizzle; the 32
+      // lanes' rows then fill all banks)
       const int m = (warp & 3) * 32 + lane;
-      const int64_t h = h0 + (m >> 6);
-      float* out = p.E + (((b * p.nc + c) * p.H + h) * kTP + (m & 63)) * N;
+      const int hh = m >> 6, r = m & 63;
       uint32_t v[N / 32][16];  // this thread's N / 2 columns: all loads, then one wait
 #pragma unroll
       for (int k = 0; k < N / 32; ++k)
         tmem_ld16_async(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + (warp >> 2) * (N / 2) + 16 * k, v[k]);
       tmem_wait();
-      if (h < p.H) {
+      unsigned char* stage = sm.Bt;
 #pragma unroll
-        for (int k = 0; k < N / 32; ++k) {
-          const int c0 = (warp >> 2) * (N / 2) + 16 * k;
+      for (int k = 0; k < N / 32; ++k) {
+        const int col = (warp >> 2) * (N / 2) + 16 * k;  // 16 columns: half of column block col / 32
+        unsigned char* row = stage + ((hh * (N / 32) + col / 32) * 64 + r) * 128;
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(out + c0 + e) =
-                make_float4(__uint_as_float(v[k][e]), __uint_as_float(v[k][e + 1]), __uint_as_float(v[k][e + 2]),
-                            __uint_as_float(v[k][e + 3]));
+        for (int e = 0; e < 16; e += 4) {
+          const int piece = ((col & 31) + e) >> 2;
+          *reinterpret_cast<float4*>(row + ((piece ^ (r & 7)) << 4)) =
+              make_float4(__uint_as_float(v[k][e]), __uint_as_float(v[k][e + 1]), __uint_as_float(v[k][e + 2]),
+                          __uint_as_float(v[k][e + 3]));
         }
+      }
+      fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int64_t h = h0 + q2;
+          if (h >= p.H) break;
+          const int erow = static_cast<int>(((b * p.nc + c) * p.H + h) * kTP);
+#pragma unroll
+          for (int cb = 0; cb < N / 32; ++cb) tma_store2(&mE, cb * 32, erow, stage + (q2 * (N / 32) + cb) * 64 * 128);
+        }
+        tma_store_drain();  // the staging tiles are read before they are reused or the CTA exits
       }
     }
     phase ^= 1u;
@@ -634,6 +669,19 @@ bool bf16_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 2-D tensor map with the 128-byte swizzle (boxes 32 columns wide): dims / box innermost first
+bool f32_map(CUtensorMap* m, const void* base, cuuint64_t cols, cuuint64_t rows, cuuint32_t box_rows) {
+  EncodeFn enc = tc_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 4};
+  const cuuint32_t box[2] = {32, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <auto Kern>
 cudaError_t tc_smem_once(size_t smem) {
   static bool set[64] = {false};
@@ -680,7 +728,7 @@ cudaError_t launch_tc_n(const SsdArgs& a) {
   p.S = reinterpret_cast<__nv_bfloat16*>(ws + lay.s_off);
   p.slast = reinterpret_cast<float*>(ws + lay.d_off);
 
-  CUtensorMap mX, mB, mC, mS;
+  CUtensorMap mX, mB, mC, mS, mE;
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.H * kTP), static_cast<cuuint64_t>(a.L),
                                 static_cast<cuuint64_t>(a.batch)};
@@ -700,12 +748,14 @@ cudaError_t launch_tc_n(const SsdArgs& a) {
     const cuuint32_t box[2] = {64, kTP};
     if (!bf16_map(&mS, p.S, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
+  if (!f32_map(&mE, p.E, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(a.batch * p.nc * a.H * kTP), kTP))
+    return cudaErrorInvalidValue;
   cudaError_t e;
   const size_t smem1 = sizeof(ChunkSmem<N>) + 1024, smem3 = sizeof(OutSmem<N>) + 1024;
   if ((e = tc_smem_once<ssd_chunk_state_kernel<N, ZOH>>(smem1)) != cudaSuccess) return e;
   if ((e = tc_smem_once<ssd_output_kernel<N, ZOH>>(smem3)) != cudaSuccess) return e;
   const int64_t g1 = ((a.H + 1) / 2 + kPairsPerCta - 1) / kPairsPerCta;
-  ssd_chunk_state_kernel<N, ZOH><<<static_cast<unsigned>(a.batch * p.nc * g1), kTT, smem1, a.stream>>>(mX, mB, p);
+  ssd_chunk_state_kernel<N, ZOH><<<static_cast<unsigned>(a.batch * p.nc * g1), kTT, smem1, a.stream>>>(mX, mB, mE, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t threads = a.batch * a.H * kTP * (N / 4);
   cudaLaunchAttribute pdl[1];
