@@ -99,10 +99,17 @@ __device__ __forceinline__ void tma_store2(const CUtensorMap* m, int c0, int c1,
                ::"l"(m), "r"(c0), "r"(c1), "r"(s32(src))
                : "memory");
 }
-// Commit the issued bulk stores and wait until they have read their shared-memory sources.
+__device__ __forceinline__ void tma_store3(const CUtensorMap* m, int c0, int c1, int c2, const void* src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+               ::"l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(s32(src))
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's committed bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void tma_store_drain() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  tma_store_commit();
+  tma_store_wait_read();
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -451,7 +458,8 @@ template <int N, bool ZOH>
 __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__ CUtensorMap mX,
                                                          const __grid_constant__ CUtensorMap mB,
                                                          const __grid_constant__ CUtensorMap mC,
-                                                         const __grid_constant__ CUtensorMap mS, TcParams p) {
+                                                         const __grid_constant__ CUtensorMap mS,
+                                                         const __grid_constant__ CUtensorMap mY, TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   OutSmem<N>& sm = *reinterpret_cast<OutSmem<N>*>(smem_raw + ((1024u - (s32(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -528,7 +536,6 @@ __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__
     if (ok && tid == 0) pendG = -1;
   }
   const int i = (warp & 3) * 32 + lane;  // this thread's row: step i of the chunk, TMEM lane i
-  const int64_t t = c * kTQ + i;
   uint32_t phase = 0;
   for (int q = 0; q < nh && ok; ++q) {
     const int64_t h = hbase + q;
@@ -542,6 +549,10 @@ __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) tmem_ld16_async(tmem + lane_base + half * 64 + 16 * g4, graw[g4]);
       tmem_wait();
+      if (q > 0) {  // BM still holds the previous head's y tile until its bulk store has read it
+        if (tid == 0) tma_store_wait_read();
+        __syncthreads();
+      }
 #pragma unroll
       for (int g4 = 0; g4 < 4; ++g4) {
         const int j0 = half * 64 + 16 * g4;
@@ -599,10 +610,11 @@ __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__
       pendM = -1;
       if (q + 1 < nh) issue_xs(h + 1, phase ^ 1u);  // the MMAs that read the x and S tiles are done
     }
-    // ---- epilogue: y = D1 + e^{s_i} D2 ----
+    // ---- epilogue: y = D1 + e^{s_i} D2, staged in BM as the [128 steps][64] bf16 box of the y tensor map
+    // (128-byte rows, 16-byte pieces XOR-swizzled by the row) and written by one bulk tensor store, which
+    // leaves out the steps past L ----
     {
       const float e = ex2(sm.s[q][i]);
-      __nv_bfloat16* yp = p.y + ((b * p.L + t) * p.H + h) * kTP;
       uint32_t d1[2][16], d2[2][16];  // this thread's 32 columns of D1 and D2: four loads, one wait
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
@@ -610,26 +622,31 @@ __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__
         tmem_ld16_async(tmem + lane_base + 192 + half * (kTP / 2) + 16 * k, d2[k]);
       }
       tmem_wait();
+      unsigned char* yrow = sm.BM + i * 128;
 #pragma unroll
       for (int k2 = 0; k2 < 2; ++k2) {
-        const int p0 = half * (kTP / 2) + 16 * k2;
+        const int piece = (half * (kTP / 2) + 16 * k2) >> 3;  // columns 8 piece .. 8 piece + 15
         uint32_t pk[8];
 #pragma unroll
         for (int k = 0; k < 16; k += 2)
           pk[k / 2] = bf2(fmaf(e, __uint_as_float(d2[k2][k]), __uint_as_float(d1[k2][k])),
                           fmaf(e, __uint_as_float(d2[k2][k + 1]), __uint_as_float(d1[k2][k + 1])));
-        if (t < p.L) {
-          *reinterpret_cast<uint4*>(yp + p0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4*>(yp + p0 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
+        *reinterpret_cast<uint4*>(yrow + ((piece ^ (i & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(yrow + (((piece + 1) ^ (i & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
+      fence_async_smem();
     }
     phase ^= 1u;
     tc_before_sync();
-    __syncthreads();  // BM and the TMEM accumulators are free for the next head
+    __syncthreads();  // the y tile is staged; the TMEM accumulators are free for the next head
     tc_after_sync();
+    if (tid == 0) {
+      tma_store3(&mY, static_cast<int>(h * kTP), static_cast<int>(c * kTQ), static_cast<int>(b), sm.BM);
+      tma_store_commit();
+    }
   }
   if (tid == 0) {  // after a wait ran out: let the copies and MMAs still in flight finish before leaving
+    tma_store_wait_read();  // and the last y tile's store read its staging
     if (pendCB >= 0) mb_wait(&sm.barCB, static_cast<uint32_t>(pendCB));
     if (pendXS >= 0) mb_wait(&sm.barXS, static_cast<uint32_t>(pendXS));
     if (pendG >= 0) mb_wait(&sm.barG, static_cast<uint32_t>(pendG));
@@ -728,13 +745,13 @@ cudaError_t launch_tc_n(const SsdArgs& a) {
   p.S = reinterpret_cast<__nv_bfloat16*>(ws + lay.s_off);
   p.slast = reinterpret_cast<float*>(ws + lay.d_off);
 
-  CUtensorMap mX, mB, mC, mS, mE;
+  CUtensorMap mX, mB, mC, mS, mE, mY;
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.H * kTP), static_cast<cuuint64_t>(a.L),
                                 static_cast<cuuint64_t>(a.batch)};
     const cuuint64_t str[2] = {static_cast<cuuint64_t>(a.H * kTP * 2), static_cast<cuuint64_t>(a.L * a.H * kTP * 2)};
     const cuuint32_t box[3] = {64, kTQ, 1};
-    if (!bf16_map(&mX, a.x, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!bf16_map(&mX, a.x, 3, dims, str, box) || !bf16_map(&mY, a.y, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(a.L), static_cast<cuuint64_t>(a.batch)};
@@ -777,7 +794,7 @@ cudaError_t launch_tc_n(const SsdArgs& a) {
   cfg3.stream = a.stream;
   cfg3.attrs = pdl;
   cfg3.numAttrs = 1;
-  if ((e = cudaLaunchKernelEx(&cfg3, ssd_output_kernel<N, ZOH>, mX, mB, mC, mS, p)) != cudaSuccess) return e;
+  if ((e = cudaLaunchKernelEx(&cfg3, ssd_output_kernel<N, ZOH>, mX, mB, mC, mS, mY, p)) != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
