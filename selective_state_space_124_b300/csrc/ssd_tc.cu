@@ -43,7 +43,7 @@ constexpr int kTP = 64;   // head dimension of this path
 constexpr int kTT = 256;  // threads per CTA: warp w reads TMEM lanes (tile rows) 32 (w % 4) .. +31 and takes
                           // column half w / 4 of them
 constexpr int kPairsPerCta = 1;  // launch 1: head pairs per CTA
-constexpr int kHeadsPerCta = 4;  // launch 3: heads per CTA
+constexpr int kHeadsPerCta = 3;  // launch 3: heads per CTA (2, 4, 6 and 8 measured slower on Mamba-2-130M)
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
 
 // ---- PTX wrappers ----------------------------------------------------------------------------------------
