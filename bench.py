@@ -786,6 +786,7 @@ def main(argv=None):
             extra["mamba130m_bwd"] = measure_backward("mamba130m", 10, flush, peak)
         if "ssd" in kinds:
             extra["mamba2_130m_ssd"] = measure_ssd("mamba2_130m", 10, flush, peak)
+            extra["mamba2_2p7b_ssd"] = measure_ssd("mamba2_2p7b", 10, flush, peak)
         if "decode" in kinds:
             extra["decode"] = measure_decode(1000, flush, peak)
         line["workloads"] = extra

@@ -44,6 +44,8 @@ WORKLOADS = {
 SSD_WORKLOADS = {
     # Mamba-2-130M-shaped layer: d_inner 1536 = 24 heads x 64, N 128
     "mamba2_130m": dict(batch=2, L=2048, H=24, P=64, N=128, disc="euler", mu=-2.0, sigma=1.0),
+    # Mamba-2-2.7B-shaped layer: d_inner 5120 = 80 heads x 64, N 128, one 8192-step sequence
+    "mamba2_2p7b": dict(batch=1, L=8192, H=80, P=64, N=128, disc="euler", mu=-2.0, sigma=1.0),
 }
 
 _CHUNK = 1 << 24

@@ -93,6 +93,30 @@ def test_ssd_mamba2_130m(orc):
     assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
 
 
+def test_ssd_mamba2_2p7b_sampled_heads(orc):
+    """The full Mamba-2-2.7B-shaped layer (batch 1, L 8192, 80 heads x 64, N 128) on the GPU; the oracle on
+    four heads (first, last, two inside), every step and state entry of those heads. Heads are independent
+    given the shared B and C, so the oracle runs on the heads' slices."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    cfg = ssm_inputs.SSD_WORKLOADS["mamba2_2p7b"]
+    batch, L, H, P, N = cfg["batch"], cfg["L"], cfg["H"], cfg["P"], cfg["N"]
+    inp = ssm_inputs.make_ssd_inputs(batch, L, H, P, N, seed=0)
+    x = _bf16(torch, inp["x_bits"], (batch, L, H, P))
+    B = _bf16(torch, inp["B_bits"], (batch, L, N))
+    C = _bf16(torch, inp["C_bits"], (batch, L, N))
+    y, fs = lib.ssm_ssd_fwd(x, torch.from_numpy(inp["delta"]).cuda(), torch.from_numpy(inp["A_log"]).cuda(), B, C,
+                            disc=cfg["disc"])
+    lib.check_device()
+    heads = [0, 29, 51, H - 1]
+    yr, sr = orc.ssd_fwd(np.ascontiguousarray(inp["x"][:, :, heads]), np.ascontiguousarray(inp["delta"][:, :, heads]),
+                         inp["A_log"][heads], inp["B"], inp["C"], disc=cfg["disc"])
+    ey = rel_err(y[:, :, heads].float().cpu().numpy(), yr)
+    es = rel_err(fs[:, heads].cpu().numpy(), sr)
+    assert ey <= TOL["bf16"], f"y rel err {ey:.3g}"
+    assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
+
+
 def test_ssd_rejects_unsupported_shapes():
     import torch
     import selective_state_space_124_b300 as lib
