@@ -132,3 +132,40 @@ def test_bwd_mamba130m_sampled(orc):
         want = ref["dA_log"][batch * j:batch * (j + 1)].sum(axis=0)
         e = rel_err(dal[dd], want)
         assert e <= TOL["f32"], f"dA_log row {dd} rel err {e:.3g}"
+
+
+def test_bwd_back_to_back_calls_reuse_outputs(orc):
+    """Two backward passes back to back into the same output buffers, through the C ABI (each call zeroes
+    dA_log, dB, dC in a kernel that its backward kernel follows as a programmatic dependent launch): the second
+    call's sums are its own, and match the oracle."""
+    import ctypes
+    import torch
+    from selective_state_space_124_b300 import _ffi
+    batch, L, D, N = 2, 900, 128, 16
+    a = ssm_inputs.make_inputs(batch, L, D, N, seed=91)
+    b = ssm_inputs.make_inputs(batch, L, D, N, seed=92)
+    rng = np.random.default_rng(93)
+    dy = [_dy(rng, (batch, L, D), "f32") for _ in range(2)]
+    out = {"dx": torch.empty((batch, L, D), device="cuda"), "ddelta": torch.empty((batch, L, D), device="cuda"),
+           "dA_log": torch.empty((D, N), device="cuda"), "dB": torch.empty((batch, L, N), device="cuda"),
+           "dC": torch.empty((batch, L, N), device="cuda"), "dh0": torch.empty((batch, D, N), device="cuda")}
+    lib = _ffi.load()
+    need = lib.ssm_scan_bwd_workspace_size(batch, L, D, N)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    v = ctypes.c_void_p
+    stream = torch.cuda.current_stream()
+    keep = []
+    for inp, g in ((a, dy[0]), (b, dy[1])):
+        d = dev_inputs(inp, "f32")
+        gd = _dev(g, "f32")
+        keep.append((d, gd))
+        st = lib.ssm_scan_bwd(v(d["x"].data_ptr()), v(d["delta"].data_ptr()), v(d["A_log"].data_ptr()),
+                              v(d["B"].data_ptr()), v(d["C"].data_ptr()), None, v(gd.data_ptr()), None,
+                              *(v(out[k].data_ptr()) for k in KEYS), v(ws.data_ptr()), ws.numel(), batch, L, D, N,
+                              _ffi.DTYPE["f32"], _ffi.DISC["euler"], v(stream.cuda_stream))
+        _ffi.check("ssm_scan_bwd", st)
+    _ffi.check("ssm_check_device", lib.ssm_check_device(v(stream.cuda_stream)))
+    ref = orc.scan_bwd(b["x"], b["delta"], b["A_log"], b["B"], b["C"], dy[1], disc="euler")
+    for k in KEYS:
+        e = rel_err(out[k].cpu().numpy(), ref[k])
+        assert e <= TOL["f32"], f"{k} rel err {e:.3g}"

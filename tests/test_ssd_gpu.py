@@ -149,3 +149,24 @@ def test_ssd_tensor_core_path_matches_warp_mma_path(orc, disc):
     yr, sr = orc.ssd_fwd(inp["x"], inp["delta"], inp["A_log"], inp["B"], inp["C"], disc=disc, h0=h0.cpu().numpy())
     assert rel_err(y1.float().cpu().numpy(), yr) <= TOL["bf16"]
     assert rel_err(f1.cpu().numpy(), sr) <= TOL["bf16"]
+
+
+def test_ssd_back_to_back_calls_share_a_workspace(orc):
+    """Two layers run back to back on one stream with one workspace (launches 2 and 3 of each call are
+    programmatic dependent launches): each result equals the same call made alone."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    batch, L, H, P, N = 2, 700, 6, 64, 128
+    ins = [ssm_inputs.make_ssd_inputs(batch, L, H, P, N, seed=s) for s in (81, 82)]
+    dev = [dict(x=_bf16(torch, i["x_bits"], (batch, L, H, P)), B=_bf16(torch, i["B_bits"], (batch, L, N)),
+                C=_bf16(torch, i["C_bits"], (batch, L, N)), dt=torch.from_numpy(i["delta"]).cuda(),
+                A=torch.from_numpy(i["A_log"]).cuda()) for i in ins]
+    ws = torch.empty(lib.ssd_workspace_size(batch, L, H, P, N), dtype=torch.uint8, device="cuda")
+    alone = []
+    for d in dev:
+        alone.append(lib.ssm_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], disc="zoh", workspace=ws))
+        torch.cuda.synchronize()
+    both = [lib.ssm_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], disc="zoh", workspace=ws) for d in dev]
+    lib.check_device()
+    for (ya, fa), (yb, fb) in zip(alone, both):
+        assert torch.equal(ya, yb) and torch.equal(fa, fb)
