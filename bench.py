@@ -779,14 +779,14 @@ def main(argv=None):
         if "prefill" in kinds:
             for name in ("long", "mamba130m", "mamba1p4b"):
                 if name != args.workload:
-                    extra[name] = measure_prefill(name, 10, flush, peak)
+                    extra[name] = measure_prefill(name, 20, flush, peak)
         if "fused" in kinds:  # the layer pieces and the backward pass on the Mamba-130M-shaped layer
             extra["mamba130m_fused"] = measure_prefill("mamba130m", 10, flush, peak, fused=True)
         if "bwd" in kinds:
-            extra["mamba130m_bwd"] = measure_backward("mamba130m", 10, flush, peak)
+            extra["mamba130m_bwd"] = measure_backward("mamba130m", 20, flush, peak)
         if "ssd" in kinds:
-            extra["mamba2_130m_ssd"] = measure_ssd("mamba2_130m", 10, flush, peak)
-            extra["mamba2_2p7b_ssd"] = measure_ssd("mamba2_2p7b", 10, flush, peak)
+            extra["mamba2_130m_ssd"] = measure_ssd("mamba2_130m", 20, flush, peak)
+            extra["mamba2_2p7b_ssd"] = measure_ssd("mamba2_2p7b", 20, flush, peak)
         if "decode" in kinds:
             extra["decode"] = measure_decode(1000, flush, peak)
         line["workloads"] = extra
