@@ -781,7 +781,7 @@ def main(argv=None):
                 if name != args.workload:
                     extra[name] = measure_prefill(name, 20, flush, peak)
         if "fused" in kinds:  # the layer pieces and the backward pass on the Mamba-130M-shaped layer
-            extra["mamba130m_fused"] = measure_prefill("mamba130m", 10, flush, peak, fused=True)
+            extra["mamba130m_fused"] = measure_prefill("mamba130m", 20, flush, peak, fused=True)
         if "bwd" in kinds:
             extra["mamba130m_bwd"] = measure_backward("mamba130m", 20, flush, peak)
         if "ssd" in kinds:
