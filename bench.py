@@ -790,7 +790,7 @@ def main(argv=None):
         if "decode" in kinds:
             extra["decode"] = measure_decode(1000, flush, peak)
         line["workloads"] = extra
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the oracle baseline is timed at N = 1 only
         line["cpu_baseline"] = cpu_baseline_subprocess(args)
     print(json.dumps(line), flush=True)
     if world > 1:
