@@ -66,6 +66,7 @@ struct BwdParams {
   int64_t groups;   // ceil(D / 32)
   int64_t total;    // batch * groups * L
   int64_t nwarps;
+  int vec;          // fp32 with D % 4 == 0 and 16-byte-aligned x, delta, dy, B, C: chunks load as float4 tiles
 };
 
 // f(w) = (w e^w - (e^w - 1)) / w^2 = sum_{m >= 2} (m - 1) w^(m-2) / m!: the Taylor series up to w^6 where the
@@ -409,14 +410,40 @@ __constant__ float2 kPairInvN1[8] = {{1.f, 1.f / 2.f},         {1.f / 3.f, 1.f /
                                      {1.f / 13.f, 1.f / 14.f}, {1.f / 15.f, 1.f / 16.f}};
 
 // A chunk's inputs held in registers between their load and their store to shared memory, so that the loads
-// of the next chunk are in flight while the current one is computed.
+// of the next chunk are in flight while the current one is computed. Two layouts: each lane's own channel for
+// the chunk's steps (x[i] = step i), or, when p.vec is set, the warp's [kChunk x 32] tiles read as float4s
+// (lane l holds columns 4 (l % 8) .. + 3 of rows l / 8 and l / 8 + 4 in x[0..3] and x[4..7]; B, C: float4 l of
+// the chunk's [kChunk x 16] rows). Both land in shared memory in the same [step][lane] layout.
 struct ChunkRegs {
   float x[kChunk], d[kChunk], g[kChunk], b[kChunk * 16 / 32], c[kChunk * 16 / 32];
 };
 
+__device__ __forceinline__ float4 ld4(const float* p, bool ok) {
+  return ok ? __ldg(reinterpret_cast<const float4*>(p)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+}
+__device__ __forceinline__ void put4(float* dst, float4 v) { dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w; }
+__device__ __forceinline__ float4 get4(const float* src) { return make_float4(src[0], src[1], src[2], src[3]); }
+
 template <typename T, bool WX, bool WG, bool WB, bool WC>
 __device__ __forceinline__ void chunk_load(const BwdParams& p, int64_t b, int64_t d, bool act, int lane, int64_t s,
                                            int n, ChunkRegs& r) {
+  static_assert(kChunk == 8, "the float4 tile layout covers 8 steps");
+  if (sizeof(T) == 4 && p.vec) {
+    const int q = lane & 7, r0 = lane >> 3;
+    const int64_t col = d - lane + 4 * q;  // first channel of this lane's float4
+    const bool cok = col < p.D;            // D % 4 == 0: a float4 is wholly inside or wholly past the row
+    const int64_t o0 = (b * p.L + s + r0) * p.D + col, o1 = o0 + 4 * p.D;
+    const bool ok0 = cok && r0 < n, ok1 = cok && r0 + 4 < n;
+    if (WX) { put4(r.x, ld4(static_cast<const float*>(p.x) + o0, ok0)); put4(r.x + 4, ld4(static_cast<const float*>(p.x) + o1, ok1)); }
+    put4(r.d, ld4(static_cast<const float*>(p.delta) + o0, ok0));
+    put4(r.d + 4, ld4(static_cast<const float*>(p.delta) + o1, ok1));
+    if (WG) { put4(r.g, ld4(static_cast<const float*>(p.dy) + o0, ok0)); put4(r.g + 4, ld4(static_cast<const float*>(p.dy) + o1, ok1)); }
+    const int64_t bc = (b * p.L + s) * 16 + 4 * lane;
+    const bool bok = (lane >> 2) < n;
+    if (WB) put4(r.b, ld4(static_cast<const float*>(p.B) + bc, bok));
+    if (WC) put4(r.c, ld4(static_cast<const float*>(p.C) + bc, bok));
+    return;
+  }
   const int64_t base = (b * p.L + s) * p.D + d;
   const int64_t bc = (b * p.L + s) * 16;
 #pragma unroll
@@ -436,19 +463,29 @@ __device__ __forceinline__ void chunk_load(const BwdParams& p, int64_t b, int64_
 }
 
 template <bool WX, bool WG, bool WB, bool WC>
-__device__ __forceinline__ void chunk_store(const ChunkRegs& r, int lane, float* xs, float* ds, float* gs, float* bs,
-                                            float* cs) {
+__device__ __forceinline__ void chunk_store(const BwdParams& p, const ChunkRegs& r, int lane, float* xs, float* ds,
+                                            float* gs, float* bs, float* cs) {
   __syncwarp();  // every lane has finished reading the previous chunk
+  if (p.vec) {
+    const int o0 = (lane >> 3) * 32 + 4 * (lane & 7), o1 = o0 + 4 * 32;
+    if (WX) { *reinterpret_cast<float4*>(xs + o0) = get4(r.x); *reinterpret_cast<float4*>(xs + o1) = get4(r.x + 4); }
+    *reinterpret_cast<float4*>(ds + o0) = get4(r.d);
+    *reinterpret_cast<float4*>(ds + o1) = get4(r.d + 4);
+    if (WG) { *reinterpret_cast<float4*>(gs + o0) = get4(r.g); *reinterpret_cast<float4*>(gs + o1) = get4(r.g + 4); }
+    if (WB) *reinterpret_cast<float4*>(bs + 4 * lane) = get4(r.b);
+    if (WC) *reinterpret_cast<float4*>(cs + 4 * lane) = get4(r.c);
+  } else {
 #pragma unroll
-  for (int i = 0; i < kChunk; ++i) {
-    if (WX) xs[i * 32 + lane] = r.x[i];
-    ds[i * 32 + lane] = r.d[i];
-    if (WG) gs[i * 32 + lane] = r.g[i];
-  }
+    for (int i = 0; i < kChunk; ++i) {
+      if (WX) xs[i * 32 + lane] = r.x[i];
+      ds[i * 32 + lane] = r.d[i];
+      if (WG) gs[i * 32 + lane] = r.g[i];
+    }
 #pragma unroll
-  for (int m = 0; m < kChunk * 16 / 32; ++m) {
-    if (WB) bs[lane + 32 * m] = r.b[m];
-    if (WC) cs[lane + 32 * m] = r.c[m];
+    for (int m = 0; m < kChunk * 16 / 32; ++m) {
+      if (WB) bs[lane + 32 * m] = r.b[m];
+      if (WC) cs[lane + 32 * m] = r.c[m];
+    }
   }
   __syncwarp();
 }
@@ -568,7 +605,7 @@ __device__ __forceinline__ void bwd_piece_s4d(const BwdParams& p, float A0, floa
     chunk_load<T, true, false, true, false>(p, b, d, act, lane, s, static_cast<int>(j - s), nx);
     while (true) {  // chunk [s, j)
       const int cn = static_cast<int>(j - s);
-      chunk_store<true, false, true, false>(nx, lane, xs, ds, gs, bs, cs);
+      chunk_store<true, false, true, false>(p, nx, lane, xs, ds, gs, bs, cs);
       const int64_t s2 = s > kChunk ? s - kChunk : 0;
       if (s > 0) chunk_load<T, true, false, true, false>(p, b, d, act, lane, s2, static_cast<int>(s - s2), nx);
       if (live == 8) s4d_walk_back<8, ZOH>(xs, ds, bs, cn, lane, A2_0, invA0, W, P, h);
@@ -610,7 +647,7 @@ __device__ __forceinline__ void bwd_piece_s4d(const BwdParams& p, float A0, floa
     chunk_load<T, true, false, true, false>(p, b, d, act, lane, s, static_cast<int>(e - s), nx);
     for (int64_t ck = ck0; ck <= ck1; ++ck) {
       span(ck, s, e);
-      chunk_store<true, false, true, false>(nx, lane, xs, ds, gs, bs, cs);
+      chunk_store<true, false, true, false>(p, nx, lane, xs, ds, gs, bs, cs);
       if (ck < ck1) {
         int64_t s2, e2;
         span(ck + 1, s2, e2);
@@ -650,7 +687,7 @@ __device__ __forceinline__ void bwd_piece_s4d(const BwdParams& p, float A0, floa
     chunk_load<T, false, true, false, true>(p, b, d, act, lane, j, static_cast<int>(e - j), nx);
     while (true) {  // chunk [j, e)
       const int cn = static_cast<int>(e - j);
-      chunk_store<false, true, false, true>(nx, lane, xs, ds, gs, bs, cs);
+      chunk_store<false, true, false, true>(p, nx, lane, xs, ds, gs, bs, cs);
       const int64_t e2 = e + kChunk < L ? e + kChunk : L;
       if (e < L) chunk_load<T, false, true, false, true>(p, b, d, act, lane, e, static_cast<int>(e2 - e), nx);
       if (live == 8) s4d_walk_fwd<8>(ds, gs, cs, cn, lane, A2_0, W, P, mu);
@@ -705,7 +742,7 @@ __device__ __forceinline__ void bwd_piece_s4d(const BwdParams& p, float A0, floa
     int64_t s, e;
     span(ck, s, e);
     const int cn = static_cast<int>(e - s);
-    chunk_store<true, true, true, true>(nx, lane, xs, ds, gs, bs, cs);
+    chunk_store<true, true, true, true>(p, nx, lane, xs, ds, gs, bs, cs);
     if (ck > ck0) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) h[k] = hn[k];
@@ -1001,6 +1038,8 @@ cudaError_t launch_bwd(const BwdArgs& a) {
   if (nw > want) nw = want;
   if (nw < 1) nw = 1;
   bp.nwarps = nw;
+  auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  bp.vec = a.dtype == 0 && a.N == 16 && a.D % 4 == 0 && a16(a.x) && a16(a.delta) && a16(a.dy) && a16(a.B) && a16(a.C);
   if (a.disc == 1)
     return a.dtype == 1 ? launch_bwd_disc<true, __nv_bfloat16>(bp, a.stream) : launch_bwd_disc<true, float>(bp, a.stream);
   return a.dtype == 1 ? launch_bwd_disc<false, __nv_bfloat16>(bp, a.stream) : launch_bwd_disc<false, float>(bp, a.stream);
