@@ -20,8 +20,10 @@
  * points can apply softplus(delta + bias) themselves.
  *
  * Conventions shared by every entry point:
- *  - Every pointer is DEVICE memory of the current CUDA device, owned by the caller. No call allocates or
- *    frees memory, and none keeps a pointer after it returns. The one exception: ssm_scan_bwd_noalloc
+ *  - Every pointer is DEVICE memory of the current CUDA device, owned by the caller, except the data arrays
+ *    of ssm_scan_fwd_host, which are host memory. No call allocates or frees memory, and none keeps a
+ *    pointer after it returns (ssm_scan_fwd_host creates two streams and a few events per device on first
+ *    use and keeps them for the process). The one exception: ssm_scan_bwd_noalloc
  *    uses a fixed 64 MiB scratch array compiled into the backward pass's device code. The CUDA runtime
  *    loads that code onto a device the first time a backward entry point (ssm_scan_bwd or
  *    ssm_scan_bwd_noalloc) runs there (module loading is lazy by default; with
@@ -218,8 +220,8 @@ ssm_status ssm_scan_bwd_noalloc(const void *x, const void *delta, const float *A
 /*
  * Mamba-2 SSD layer: the scan with A = a I, one scalar a per head, evaluated in chunks ("State Space Models
  * & Mamba" chapter, the Mamba-2 paragraph; "Mathematical Prerequisites for Mamba" s7: the recurrence is a
- * 1-semiseparable matrix product, computed as masked matrix products inside chunks of 64 steps on the
- * tensor cores, with the recurrence carrying the state between chunks). For head h with state S [P, N]:
+ * 1-semiseparable matrix product, computed as masked matrix products inside chunks on the tensor cores, with
+ * the recurrence carrying the state between chunks). For head h with state S [P, N]:
  *   A_h = -exp(A_log[h]),  Abar = exp(delta[b,t,h] A_h),  coef = delta (Euler) or (Abar - 1) / A_h (ZOH)
  *   S[p][n] = Abar S[p][n] + coef B[b,t,n] x[b,t,h,p],   y[b,t,h,p] = sum_n C[b,t,n] S[p][n]
  *   x, y        [batch, L, H, P]  bf16 (dtype must be SSM_DTYPE_BF16)
@@ -228,23 +230,32 @@ ssm_status ssm_scan_bwd_noalloc(const void *x, const void *delta, const float *A
  *   B, C        [batch, L, N]     bf16, one group shared by every head
  *   h0          [batch, H, P, N]  fp32 initial state, or NULL
  *   final_state [batch, H, P, N]  fp32, or NULL
- *   workspace   device memory of ssm_ssd_fwd_workspace_size() bytes, or NULL. With it, each sequence is
- *               cut into segments that separate CTAs scan from a zero state, and a second pass adds the
- *               state carried into each segment. Without it (or when it is too small), one CTA walks each
- *               sequence. Both give the same function. Its contents on entry do not matter. Two calls in
- *               flight may not share it.
+ *   workspace   device memory of ssm_ssd_fwd_workspace_size() bytes, or NULL; its contents on entry do not
+ *               matter, and two calls in flight may not share it.
+ * Two implementations, the same function:
+ *  - P = 64 with a workspace of at least ssm_ssd_fwd_workspace_size() bytes (256-byte aligned; h0 and
+ *    final_state 16-byte aligned): chunks of 128 steps in parallel on the fifth-generation tensor cores
+ *    (tcgen05 MMAs with TMEM accumulators, bulk tensor copies), in three launches on `stream` -- the chunks'
+ *    own states into the workspace, the recurrence between chunks, the outputs. The second and third are
+ *    programmatic dependent launches of the one before (each waits for its predecessor's writes before
+ *    reading them); ordering against other work on `stream` is that of ordinary launches.
+ *  - otherwise: chunks of 64 steps with warp-level MMAs, one CTA per (batch element, head, 16 channels)
+ *    walking the sequence; with a workspace, long sequences are cut into segments scanned from a zero state
+ *    and a second pass adds the state carried into each.
  * N must be 64 or 128 and P a multiple of 16 (else SSM_ERR_UNSUPPORTED); x, B, C and y must be 16-byte
  * aligned (else SSM_ERR_UNSUPPORTED). The products run with bf16 operands and fp32 accumulation (the
  * masked score tile and a bf16 copy of the carried state are rounded to bf16 as operands; the state itself
- * is carried in fp32). Other conventions as for ssm_scan_fwd.
+ * is carried in fp32). A bounded wait of the tensor-core kernels that runs out (2 s) is reported by
+ * ssm_check_device() as SSM_ERR_TIMEOUT. Other conventions as for ssm_scan_fwd.
  */
 ssm_status ssm_ssd_fwd(const void *x, const float *delta, const float *A_log, const void *B, const void *C,
                        const float *h0, void *y, float *final_state, void *workspace, size_t workspace_bytes,
                        int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N,
                        ssm_dtype dtype, ssm_disc disc, void *stream);
 
-/* Bytes of workspace that let ssm_ssd_fwd cut long sequences into segments scanned in parallel (on the current
-   device; 0 when one CTA per sequence already fills it, or for unsupported shapes). */
+/* Bytes of workspace for ssm_ssd_fwd: for P = 64, the chunk states, the states entering each chunk and each
+   chunk's log decay of the tensor-core path; for other P, the segment states of the warp-MMA path on the current
+   device (0 when one CTA per sequence already fills it). 0 for unsupported shapes. */
 size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N);
 
 /* Synchronise `stream` and report any error raised while this library's kernels ran on it. */
