@@ -301,9 +301,12 @@ def measure_prefill(name, reps, flush, peak, fused=False):
     nbytes = fwd_bytes(cfg) + ((b * L * D * es + 2 * D * 4) if fused else 0)  # + z, bias, D
     gbs = nbytes / med / 1e9
     what = describe(name, cfg).split(";")[0] + ("; fused softplus(delta + bias), + D x, * SiLU(z)" if fused else "")
-    return {"workload": what, "launch_ms_median": med * 1e3, "elems_per_s": b * L * D / med, "gbs": gbs,
-            "hbm_frac": gbs / peak, "bytes_per_launch": nbytes, "reps": reps,
-            "traffic": None if fused else ncu_traffic("scan_fwd", name)}
+    out = {"workload": what, "launch_ms_median": med * 1e3, "elems_per_s": b * L * D / med, "gbs": gbs,
+           "hbm_frac": gbs / peak, "bytes_per_launch": nbytes, "reps": reps,
+           "traffic": None if fused else ncu_traffic("scan_fwd", name)}
+    if nbytes < (1 << 20):  # the tiny scan moves kilobytes: its time is launch latency, not a roofline figure
+        out["bound"] = "launch latency (no roofline gate)"
+    return out
 
 
 def measure_backward(name, reps, flush, peak):
@@ -777,7 +780,7 @@ def main(argv=None):
         kinds = set(args.extra.split(",")) if args.extra != "all" else {"prefill", "fused", "bwd", "ssd", "decode"}
         extra = {}
         if "prefill" in kinds:
-            for name in ("long", "mamba130m", "mamba1p4b"):
+            for name in ("long", "mamba130m", "mamba1p4b", "tiny"):
                 if name != args.workload:
                     extra[name] = measure_prefill(name, 20, flush, peak)
         if "fused" in kinds:  # the layer pieces and the backward pass on the Mamba-130M-shaped layer
