@@ -245,7 +245,8 @@ ssm_status ssm_scan_bwd_noalloc(const void *x, const void *delta, const float *A
  * N must be 64 or 128 and P a multiple of 16 (else SSM_ERR_UNSUPPORTED); x, B, C and y must be 16-byte
  * aligned (else SSM_ERR_UNSUPPORTED). The products run with bf16 operands and fp32 accumulation (the
  * masked score tile and a bf16 copy of the carried state are rounded to bf16 as operands; the state itself
- * is carried in fp32). A bounded wait of the tensor-core kernels that runs out (2 s) is reported by
+ * is carried in fp32; on the tensor-core path each chunk's own state, formed from bf16 operands, is stored
+ * in bf16 between the first two launches). A bounded wait of the tensor-core kernels that runs out (2 s) is reported by
  * ssm_check_device() as SSM_ERR_TIMEOUT. Other conventions as for ssm_scan_fwd.
  */
 ssm_status ssm_ssd_fwd(const void *x, const float *delta, const float *A_log, const void *B, const void *C,
@@ -253,8 +254,8 @@ ssm_status ssm_ssd_fwd(const void *x, const float *delta, const float *A_log, co
                        int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N,
                        ssm_dtype dtype, ssm_disc disc, void *stream);
 
-/* Bytes of workspace for ssm_ssd_fwd: for P = 64, the chunk states, the states entering each chunk and each
-   chunk's log decay of the tensor-core path; for other P, the segment states of the warp-MMA path on the current
+/* Bytes of workspace for ssm_ssd_fwd: for P = 64, the chunk states and the states entering each chunk (bf16)
+   and each chunk's log decay (fp32) of the tensor-core path; for other P, the segment states of the warp-MMA path on the current
    device (0 when one CTA per sequence already fills it). 0 for unsupported shapes. */
 size_t ssm_ssd_fwd_workspace_size(int64_t batch, int64_t L, int64_t H, int64_t P, int64_t N);
 

@@ -13,9 +13,10 @@
 //   1. ssd_chunk_state_kernel: one CTA per (batch element, chunk, group of head pairs). Per head pair, E for
 //      both heads is one MMA chain: M = 128 rows (head, p), N = state size, K = the chunk's 128 steps, A = the
 //      x tile scaled by e^{s_last - s_j} coef_j (read in its natural layout, MN-major), B = the chunk's B tile
-//      (natural layout, MN-major). E goes to the workspace in fp32.
-//   2. ssd_state_pass_kernel: the recurrence between chunks, elementwise over (b, h, p, n); writes every S_c in
-//      bf16 (the operand of launch 3) and the final state in fp32.
+//      (natural layout, MN-major). E goes to the workspace in bf16 (the precision of the operands it is formed
+//      from; it is the largest intermediate, and half the bytes cut the traffic of launches 1 and 2).
+//   2. ssd_state_pass_kernel: the recurrence between chunks in fp32, elementwise over (b, h, p, n); writes every
+//      S_c in bf16 (the operand of launch 3) and the final state in fp32.
 //   3. ssd_output_kernel: one CTA per (batch element, chunk, group of heads). G = C B^T (M = N = 128, K = state
 //      size) is formed once and shared by the group's heads; per head the mask-and-decay of G is written to
 //      shared memory in bf16 (A operand), and two MMA chains give D1 = (G o L) X (B = the x tile, MN-major) and
@@ -170,7 +171,7 @@ struct TcParams {
   const float* h0;      // [batch, H, 64, N] or null
   __nv_bfloat16* y;     // [batch, L, H, 64]
   float* final_state;   // [batch, H, 64, N] or null
-  float* E;             // workspace: [batch, nc, H, 64, N] fp32 chunk states
+  __nv_bfloat16* E;     // workspace: [batch, nc, H, 64, N] bf16 chunk states
   __nv_bfloat16* S;     // workspace: [batch, nc, H, 64, N] bf16 states entering each chunk
   float* slast;         // workspace: [batch, nc, H] total log decay of each chunk
   int64_t batch, L, H, nc;
@@ -236,12 +237,12 @@ template <int N, bool ZOH>
 __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_constant__ CUtensorMap mX,
                                                               const __grid_constant__ CUtensorMap mB,
                                                               const __grid_constant__ CUtensorMap mE, TcParams p) {
-  // E leaves through shared memory: the B and x tiles (contiguous, free once the MMA is done) hold the pair's
-  // [2 heads][N / 32 column blocks][64 rows][32 fp32] boxes, which bulk tensor stores write to the workspace.
-  // The B tile is loaded once per CTA, so this needs one head pair per CTA.
+  // E leaves through shared memory: the B tile (free once the MMA is done) holds the pair's [2 heads][N / 64
+  // column blocks][64 rows][64 bf16] boxes, which bulk tensor stores write to the workspace. E is rounded to
+  // bf16 there, like the tensor-core operands it is formed from (the x tile scaled by its decay weights). The
+  // B tile is loaded once per CTA, so this needs one head pair per CTA.
   static_assert(kPairsPerCta == 1, "the E staging reuses the B tile");
-  static_assert(offsetof(ChunkSmem<N>, Xt) == N * 256 && N * 256 + 2 * kTQ * 128 >= 2 * kTP * N * 4,
-                "the B and x tiles must be contiguous and hold the pair's E");
+  static_assert(N * 256 >= 2 * kTP * N * 2, "the B tile must hold the pair's E in bf16");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   ChunkSmem<N>& sm = *reinterpret_cast<ChunkSmem<N>*>(smem_raw + ((1024u - (s32(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -342,9 +343,9 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
     if (!ok) break;
     if (tid == 0) pendM = -1;
     {
-      // row m of D is head h0 + m / 64, channel p = m % 64: its N entries of E go to the staging boxes, rows of
-      // 128 bytes whose 16-byte pieces are XOR-swizzled by the row (the tensor map's 128-byte swizzle; the 32
-      // lanes' rows then fill all banks)
+      // row m of D is head h0 + m / 64, channel p = m % 64: its N entries of E go to the staging boxes as bf16,
+      // rows of 128 bytes whose 16-byte pieces are XOR-swizzled by the row (the tensor map's 128-byte swizzle;
+      // the 32 lanes' rows then fill all banks)
       const int m = (warp & 3) * 32 + lane;
       const int hh = m >> 6, r = m & 63;
       uint32_t v[N / 32][16];  // this thread's N / 2 columns: all loads, then one wait
@@ -355,15 +356,14 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
       unsigned char* stage = sm.Bt;
 #pragma unroll
       for (int k = 0; k < N / 32; ++k) {
-        const int col = (warp >> 2) * (N / 2) + 16 * k;  // 16 columns: half of column block col / 32
-        unsigned char* row = stage + ((hh * (N / 32) + col / 32) * 64 + r) * 128;
+        const int col = (warp >> 2) * (N / 2) + 16 * k;  // 16 columns: a quarter of column block col / 64
+        unsigned char* row = stage + ((hh * (N / 64) + col / 64) * 64 + r) * 128;
+        const int piece = (col & 63) >> 3;  // two 16-byte pieces: columns col .. col + 7, col + 8 .. col + 15
+        uint32_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const int piece = ((col & 31) + e) >> 2;
-          *reinterpret_cast<float4*>(row + ((piece ^ (r & 7)) << 4)) =
-              make_float4(__uint_as_float(v[k][e]), __uint_as_float(v[k][e + 1]), __uint_as_float(v[k][e + 2]),
-                          __uint_as_float(v[k][e + 3]));
-        }
+        for (int e = 0; e < 8; ++e) pk[e] = bf2(__uint_as_float(v[k][2 * e]), __uint_as_float(v[k][2 * e + 1]));
+        *reinterpret_cast<uint4*>(row + ((piece ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(row + (((piece + 1) ^ (r & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
       }
       fence_async_smem();
       __syncthreads();
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
           if (h >= p.H) break;
           const int erow = static_cast<int>(((b * p.nc + c) * p.H + h) * kTP);
 #pragma unroll
-          for (int cb = 0; cb < N / 32; ++cb) tma_store2(&mE, cb * 32, erow, stage + (q2 * (N / 32) + cb) * 64 * 128);
+          for (int cb = 0; cb < N / 64; ++cb) tma_store2(&mE, cb * 64, erow, stage + (q2 * (N / 64) + cb) * 64 * 128);
         }
         tma_store_drain();  // the staging tiles are read before they are reused or the CTA exits
       }
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(256, 4) ssd_state_pass_kernel(TcParams p) {
   const int64_t row = (b * p.H + h) * kTP + pp;  // (b, h, p) of h0 / final_state
   float4 s = p.h0 ? *reinterpret_cast<const float4*>(p.h0 + row * N + 4 * n4) : make_float4(0.f, 0.f, 0.f, 0.f);
   // (b, c, h, p) rows of E / S and (b, c, h) entries of slast step by H * 64 rows and H entries per chunk
-  const float* ep = p.E + ((b * p.nc * p.H + h) * kTP + pp) * N + 4 * n4;
+  const __nv_bfloat16* ep = p.E + ((b * p.nc * p.H + h) * kTP + pp) * N + 4 * n4;
   __nv_bfloat16* sp = p.S + ((b * p.nc * p.H + h) * kTP + pp) * N + 4 * n4;
   const float* dp = p.slast + b * p.nc * p.H + h;
   const int64_t estep = p.H * kTP * N;
@@ -418,7 +418,9 @@ __global__ void __launch_bounds__(256, 4) ssd_state_pass_kernel(TcParams p) {
 #pragma unroll
     for (int k = 0; k < kAhead; ++k) {
       if (k < n) {
-        e[k] = *reinterpret_cast<const float4*>(ep + k * estep);
+        const uint2 u = *reinterpret_cast<const uint2*>(ep + k * estep);  // four bf16
+        e[k] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
         dl[k] = dp[k * p.H];
       }
     }
@@ -686,19 +688,6 @@ bool bf16_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 2-D tensor map with the 128-byte swizzle (boxes 32 columns wide): dims / box innermost first
-bool f32_map(CUtensorMap* m, const void* base, cuuint64_t cols, cuuint64_t rows, cuuint32_t box_rows) {
-  EncodeFn enc = tc_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 4};
-  const cuuint32_t box[2] = {32, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <auto Kern>
 cudaError_t tc_smem_once(size_t smem) {
   static bool set[64] = {false};
@@ -721,7 +710,7 @@ TcLayout tc_layout(int64_t batch, int64_t L, int64_t H, int64_t N) {
   const size_t states = static_cast<size_t>(batch) * nc * H * kTP * N;
   TcLayout t;
   t.e_off = 0;
-  t.s_off = states * 4;
+  t.s_off = ((states * 2 + 255) / 256) * 256;
   t.d_off = t.s_off + ((states * 2 + 255) / 256) * 256;
   t.bytes = t.d_off + static_cast<size_t>(batch) * nc * H * 4;
   return t;
@@ -741,7 +730,7 @@ cudaError_t launch_tc_n(const SsdArgs& a) {
   p.nc = (a.L + kTQ - 1) / kTQ;
   const TcLayout lay = tc_layout(a.batch, a.L, a.H, N);
   unsigned char* ws = static_cast<unsigned char*>(a.workspace);
-  p.E = reinterpret_cast<float*>(ws + lay.e_off);
+  p.E = reinterpret_cast<__nv_bfloat16*>(ws + lay.e_off);
   p.S = reinterpret_cast<__nv_bfloat16*>(ws + lay.s_off);
   p.slast = reinterpret_cast<float*>(ws + lay.d_off);
 
@@ -759,14 +748,12 @@ cudaError_t launch_tc_n(const SsdArgs& a) {
     const cuuint32_t box[3] = {64, kTQ, 1};
     if (!bf16_map(&mB, a.B, 3, dims, str, box) || !bf16_map(&mC, a.C, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
-  {
+  {  // S (read by launch 3) and E (written by launch 1): [rows (b, c, h, p)][N] bf16, boxes of 64 x 64
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(a.batch * p.nc * a.H * kTP)};
     const cuuint64_t str[1] = {static_cast<cuuint64_t>(N * 2)};
     const cuuint32_t box[2] = {64, kTP};
-    if (!bf16_map(&mS, p.S, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!bf16_map(&mS, p.S, 2, dims, str, box) || !bf16_map(&mE, p.E, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
-  if (!f32_map(&mE, p.E, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(a.batch * p.nc * a.H * kTP), kTP))
-    return cudaErrorInvalidValue;
   cudaError_t e;
   const size_t smem1 = sizeof(ChunkSmem<N>) + 1024, smem3 = sizeof(OutSmem<N>) + 1024;
   if ((e = tc_smem_once<ssd_chunk_state_kernel<N, ZOH>>(smem1)) != cudaSuccess) return e;
