@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kTT) ssd_chunk_state_kernel(const __grid_const
 // ---- launch 2: the recurrence between chunks ---------------------------------------------------------------
 // One thread per (b, h, p, 4 consecutive n).
 template <int N>
-__global__ void __launch_bounds__(256, 4) ssd_state_pass_kernel(TcParams p) {
+__global__ void __launch_bounds__(256, 2) ssd_state_pass_kernel(TcParams p) {
   pdl_wait();  // E and slast of launch 1
   const int64_t total = p.batch * p.H * kTP * (N / 4);
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -410,17 +410,17 @@ __global__ void __launch_bounds__(256, 4) ssd_state_pass_kernel(TcParams p) {
   __nv_bfloat16* sp = p.S + ((b * p.nc * p.H + h) * kTP + pp) * N + 4 * n4;
   const float* dp = p.slast + b * p.nc * p.H + h;
   const int64_t estep = p.H * kTP * N;
-  constexpr int kAhead = 8;  // chunks whose E and decay are loaded together, ahead of the dependent updates
+  // chunks whose E (kept packed until used) and decay are loaded together, ahead of the dependent updates:
+  // 16 at up to 128 registers measured 8% faster on a 64-chunk sequence than 8 at 64 registers
+  constexpr int kAhead = 16;
   for (int64_t c0 = 0; c0 < p.nc; c0 += kAhead) {
     const int n = p.nc - c0 < kAhead ? static_cast<int>(p.nc - c0) : kAhead;
-    float4 e[kAhead];
+    uint2 e[kAhead];  // four bf16 each, widened where they are used
     float dl[kAhead];
 #pragma unroll
     for (int k = 0; k < kAhead; ++k) {
       if (k < n) {
-        const uint2 u = *reinterpret_cast<const uint2*>(ep + k * estep);  // four bf16
-        e[k] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                           __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+        e[k] = *reinterpret_cast<const uint2*>(ep + k * estep);
         dl[k] = dp[k * p.H];
       }
     }
@@ -432,8 +432,10 @@ __global__ void __launch_bounds__(256, 4) ssd_state_pass_kernel(TcParams p) {
         packed.y = bf2(s.z, s.w);
         *reinterpret_cast<uint2*>(sp + k * estep) = packed;
         const float dec = ex2(dl[k] * kLog2e);
-        s = make_float4(fmaf(dec, s.x, e[k].x), fmaf(dec, s.y, e[k].y), fmaf(dec, s.z, e[k].z),
-                        fmaf(dec, s.w, e[k].w));
+        s = make_float4(fmaf(dec, s.x, __uint_as_float(e[k].x << 16)),
+                        fmaf(dec, s.y, __uint_as_float(e[k].x & 0xffff0000u)),
+                        fmaf(dec, s.z, __uint_as_float(e[k].y << 16)),
+                        fmaf(dec, s.w, __uint_as_float(e[k].y & 0xffff0000u)));
       }
     }
     ep += kAhead * estep;
