@@ -44,7 +44,10 @@ constexpr int kTP = 64;   // head dimension of this path
 constexpr int kTT = 256;  // threads per CTA: warp w reads TMEM lanes (tile rows) 32 (w % 4) .. +31 and takes
                           // column half w / 4 of them
 constexpr int kPairsPerCta = 1;  // launch 1: head pairs per CTA
-constexpr int kHeadsPerCta = 3;  // launch 3: heads per CTA (2, 4, 6 and 8 measured slower on Mamba-2-130M)
+// launch 3: heads per CTA. 3 where the grid fits the resident CTAs about once (Mamba-2-130M: 2, 4, 6 and 8
+// measured slower); 6 where it would take several waves (Mamba-2-2.7B: 4% faster than 3), so that the per-CTA
+// setup (TMEM allocation, C and B tiles, G) is shared by more heads.
+constexpr int kHeadsFew = 3, kHeadsMany = 6;
 constexpr unsigned long long kTcWaitNs = 2000000000ull;
 
 // ---- PTX wrappers ----------------------------------------------------------------------------------------
@@ -446,31 +449,32 @@ __global__ void __launch_bounds__(256, 2) ssd_state_pass_kernel(TcParams p) {
 }
 
 // ---- launch 3: outputs -----------------------------------------------------------------------------------
-template <int N>
+template <int N, int HPC>
 struct OutSmem {
   alignas(1024) unsigned char Ct[N * 256];            // C tile [128 steps][N] (K-major A operand)
   alignas(1024) unsigned char BM[kTQ * 256];          // B tile [128][N] for G, then the masked G tile [128][128]
   alignas(1024) unsigned char Xt[kTQ * 128];          // x tile of one head [128 steps][64] (MN-major B operand)
   alignas(1024) unsigned char St[kTP * N * 2];        // S_c of one head [64 p][N] (K-major B operand)
-  float s[kHeadsPerCta][kTQ];                         // log2 of the decay from the chunk start through step i
-  float cf[kHeadsPerCta][kTQ];                        // input coefficient of step j
+  float s[HPC][kTQ];                                  // log2 of the decay from the chunk start through step i
+  float cf[HPC][kTQ];                                 // input coefficient of step j
   unsigned long long barCB, barXS, barG, barM;
   uint32_t tmem;
 };
 
-template <int N, bool ZOH>
+template <int N, bool ZOH, int HPC>
 __global__ void __launch_bounds__(kTT) ssd_output_kernel(const __grid_constant__ CUtensorMap mX,
                                                          const __grid_constant__ CUtensorMap mB,
                                                          const __grid_constant__ CUtensorMap mC,
                                                          const __grid_constant__ CUtensorMap mS,
                                                          const __grid_constant__ CUtensorMap mY, TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  OutSmem<N>& sm = *reinterpret_cast<OutSmem<N>*>(smem_raw + ((1024u - (s32(smem_raw) & 1023u)) & 1023u));
+  static_assert(HPC <= kTT / 32, "one warp loads each head's deltas");
+  OutSmem<N, HPC>& sm = *reinterpret_cast<OutSmem<N, HPC>*>(smem_raw + ((1024u - (s32(smem_raw) & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t groups = (p.H + kHeadsPerCta - 1) / kHeadsPerCta;
+  const int64_t groups = (p.H + HPC - 1) / HPC;
   const int64_t g = blockIdx.x % groups, c = (blockIdx.x / groups) % p.nc, b = blockIdx.x / groups / p.nc;
-  const int64_t hbase = g * kHeadsPerCta;
-  const int nh = static_cast<int>(p.H - hbase < kHeadsPerCta ? p.H - hbase : kHeadsPerCta);
+  const int64_t hbase = g * HPC;
+  const int nh = static_cast<int>(p.H - hbase < HPC ? p.H - hbase : HPC);
   constexpr uint32_t kXSBytes = kTQ * 128 + kTP * N * 2;
 
   if (tid == 0) {
@@ -718,6 +722,23 @@ TcLayout tc_layout(int64_t batch, int64_t L, int64_t H, int64_t N) {
   return t;
 }
 
+template <int N, bool ZOH, int HPC>
+cudaError_t launch_out(const SsdArgs& a, const TcParams& p, const CUtensorMap& mX, const CUtensorMap& mB,
+                       const CUtensorMap& mC, const CUtensorMap& mS, const CUtensorMap& mY,
+                       cudaLaunchAttribute* pdl) {
+  const size_t smem3 = sizeof(OutSmem<N, HPC>) + 1024;
+  cudaError_t e = tc_smem_once<ssd_output_kernel<N, ZOH, HPC>>(smem3);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg3 = {};
+  cfg3.gridDim = dim3(static_cast<unsigned>(a.batch * p.nc * ((a.H + HPC - 1) / HPC)));
+  cfg3.blockDim = dim3(kTT);
+  cfg3.dynamicSmemBytes = smem3;
+  cfg3.stream = a.stream;
+  cfg3.attrs = pdl;
+  cfg3.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg3, ssd_output_kernel<N, ZOH, HPC>, mX, mB, mC, mS, mY, p);
+}
+
 template <int N, bool ZOH>
 cudaError_t launch_tc_n(const SsdArgs& a) {
   TcParams p;
@@ -757,9 +778,8 @@ cudaError_t launch_tc_n(const SsdArgs& a) {
     if (!bf16_map(&mS, p.S, 2, dims, str, box) || !bf16_map(&mE, p.E, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   cudaError_t e;
-  const size_t smem1 = sizeof(ChunkSmem<N>) + 1024, smem3 = sizeof(OutSmem<N>) + 1024;
+  const size_t smem1 = sizeof(ChunkSmem<N>) + 1024;
   if ((e = tc_smem_once<ssd_chunk_state_kernel<N, ZOH>>(smem1)) != cudaSuccess) return e;
-  if ((e = tc_smem_once<ssd_output_kernel<N, ZOH>>(smem3)) != cudaSuccess) return e;
   const int64_t g1 = ((a.H + 1) / 2 + kPairsPerCta - 1) / kPairsPerCta;
   ssd_chunk_state_kernel<N, ZOH><<<static_cast<unsigned>(a.batch * p.nc * g1), kTT, smem1, a.stream>>>(mX, mB, mE, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -775,15 +795,13 @@ cudaError_t launch_tc_n(const SsdArgs& a) {
   cfg2.numAttrs = 1;
   if ((e = cudaLaunchKernelEx(&cfg2, ssd_state_pass_kernel<N>, p)) != cudaSuccess) return e;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int64_t g3 = (a.H + kHeadsPerCta - 1) / kHeadsPerCta;
-  cudaLaunchConfig_t cfg3 = {};
-  cfg3.gridDim = dim3(static_cast<unsigned>(a.batch * p.nc * g3));
-  cfg3.blockDim = dim3(kTT);
-  cfg3.dynamicSmemBytes = smem3;
-  cfg3.stream = a.stream;
-  cfg3.attrs = pdl;
-  cfg3.numAttrs = 1;
-  if ((e = cudaLaunchKernelEx(&cfg3, ssd_output_kernel<N, ZOH>, mX, mB, mC, mS, mY, p)) != cudaSuccess) return e;
+  // launch 3: few heads per CTA unless that grid would need more than two rounds of the two CTAs an SM holds
+  const int64_t few = a.batch * p.nc * ((a.H + kHeadsFew - 1) / kHeadsFew);
+  if (few <= 4 * static_cast<int64_t>(sm_count()))
+    e = launch_out<N, ZOH, kHeadsFew>(a, p, mX, mB, mC, mS, mY, pdl);
+  else
+    e = launch_out<N, ZOH, kHeadsMany>(a, p, mX, mB, mC, mS, mY, pdl);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
