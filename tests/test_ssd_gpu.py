@@ -117,6 +117,31 @@ def test_ssd_mamba2_2p7b_sampled_heads(orc):
     assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
 
 
+def test_ssd_six_heads_per_cta_zoh_h0_sampled_heads(orc):
+    """A layer whose three-heads-per-CTA output grid would take several waves (batch 4, L 8192, 12 heads x 64,
+    N 64: 1024 CTAs), so the output kernel takes six heads per CTA, here in two full groups; ZOH with an
+    initial state. The oracle on two heads, one from each group, every step and state entry."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    batch, L, H, P, N = 4, 8192, 12, 64, 64
+    inp = ssm_inputs.make_ssd_inputs(batch, L, H, P, N, seed=6, mu=-3.0, sigma=1.0)
+    h0 = np.random.default_rng(66).standard_normal((batch, H, P, N)).astype(np.float32)
+    x = _bf16(torch, inp["x_bits"], (batch, L, H, P))
+    B = _bf16(torch, inp["B_bits"], (batch, L, N))
+    C = _bf16(torch, inp["C_bits"], (batch, L, N))
+    y, fs = lib.ssm_ssd_fwd(x, torch.from_numpy(inp["delta"]).cuda(), torch.from_numpy(inp["A_log"]).cuda(), B, C,
+                            disc="zoh", h0=torch.from_numpy(h0).cuda())
+    lib.check_device()
+    heads = [2, 9]
+    yr, sr = orc.ssd_fwd(np.ascontiguousarray(inp["x"][:, :, heads]), np.ascontiguousarray(inp["delta"][:, :, heads]),
+                         inp["A_log"][heads], inp["B"], inp["C"], disc="zoh",
+                         h0=np.ascontiguousarray(h0[:, heads]))
+    ey = rel_err(y[:, :, heads].float().cpu().numpy(), yr)
+    es = rel_err(fs[:, heads].cpu().numpy(), sr)
+    assert ey <= TOL["bf16"], f"y rel err {ey:.3g}"
+    assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
+
+
 def test_ssd_rejects_unsupported_shapes():
     import torch
     import selective_state_space_124_b300 as lib
