@@ -783,8 +783,9 @@ def main(argv=None):
             for name in ("long", "mamba130m", "mamba1p4b", "tiny"):
                 if name != args.workload:
                     extra[name] = measure_prefill(name, 20, flush, peak)
-        if "fused" in kinds:  # the layer pieces and the backward pass on the Mamba-130M-shaped layer
+        if "fused" in kinds:  # the layer pieces on the Mamba-130M (fp32) and Mamba-1.4B (bf16) layers
             extra["mamba130m_fused"] = measure_prefill("mamba130m", 20, flush, peak, fused=True)
+            extra["mamba1p4b_fused"] = measure_prefill("mamba1p4b", 20, flush, peak, fused=True)
         if "bwd" in kinds:
             extra["mamba130m_bwd"] = measure_backward("mamba130m", 20, flush, peak)
         if "ssd" in kinds:

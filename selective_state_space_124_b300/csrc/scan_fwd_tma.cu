@@ -464,8 +464,11 @@ template <bool S4D, typename T, bool ZOH, int CPL, int TS, int NSF, int TSW, int
 __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r, const TmaParams& p,
                                           const CUtensorMap* mx, const CUtensorMap* md, const CUtensorMap* mB,
                                           int lane, int64_t row, int64_t t0, int64_t t1, WarpPipe& wp,
-                                          IssueFwd& issue_fwd, int kiss0) {
+                                          IssueFwd& issue_fwd, int kiss0, const T* zr) {
   constexpr int CW = 32 * CPL;
+  // bf16 inputs with the gate: z comes through the forward ring (zr: this warp's NSF stages of [TS][CW]
+  // tiles); fp32 inputs load each stage's z up front from global memory (their shared memory is full).
+  constexpr bool kZs = EPI == 2 && sizeof(T) == 2;
   constexpr bool kConv = sizeof(T) == 2;  // bf16: consumers read B and C from the widened Bf / Cf
   constexpr uint32_t kWarmBytes = (2u * TSW * CW + TSW * 16) * sizeof(T);
   const int64_t L = p.L;
@@ -674,7 +677,9 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
         fwd_s4d<ZOH, CPL>(xv, dv, Bs + i * 16, Cs + i * 16, A2_0, invA0, h, yv);
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-          const float zv = (EPI == 2 && act[c]) ? tof<T>(zp[static_cast<int64_t>(i) * p.D + 32 * c]) : 0.0f;
+          float zv = 0.0f;
+          if constexpr (kZs) zv = tof<T>(zr[slot * TS * CW + i * CW + c * 32 + lane]);
+          else if (EPI == 2 && act[c]) zv = tof<T>(zp[static_cast<int64_t>(i) * p.D + 32 * c]);
           yv[c] = epilogue<EPI>(yv[c], xv[c], dskip[c], zv);
           if constexpr (decltype(all_active)::value) store_y(yp + 32 * c, yv[c]);
           else store_y(yp + 32 * c, yv[c], act[c]);
@@ -744,7 +749,9 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
           const float xv = tof<T>(xs[i * CW + c * 32 + lane]);
           const float yv = fwd_gen<ZOH>(xv, delta_in<DX>(tof<T>(ds[i * CW + c * 32 + lane]), dbias[c]),
                                         Bs + i * 16, Cs + i * 16, g[S4D ? 0 : c], h[c]);
-          const float zv = (EPI == 2 && act[c]) ? tof<T>(zp[static_cast<int64_t>(i) * p.D + 32 * c]) : 0.0f;
+          float zv = 0.0f;
+          if constexpr (kZs) zv = tof<T>(zr[slot * TS * CW + i * CW + c * 32 + lane]);
+          else if (EPI == 2 && act[c]) zv = tof<T>(zp[static_cast<int64_t>(i) * p.D + 32 * c]);
           store_y(yp + 32 * c, epilogue<EPI>(yv, xv, dskip[c], zv), act[c]);
         }
         yp += p.D;
@@ -776,22 +783,25 @@ __global__ void __maxnreg__(sizeof(T) == 4 ? 240 : 168)
 scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap md,
                     const __grid_constant__ CUtensorMap mB, const __grid_constant__ CUtensorMap mC,
                     const __grid_constant__ CUtensorMap mxw, const __grid_constant__ CUtensorMap mdw,
-                    const __grid_constant__ CUtensorMap mBw, TmaParams p) {
+                    const __grid_constant__ CUtensorMap mBw, const __grid_constant__ CUtensorMap mz,
+                    TmaParams p) {
   using R = WarpRing<T, CPL, TS, NSF, TSW, NSW>;
   constexpr int CW = R::CW;
-  constexpr uint32_t kFwdBytes = (2u * TS * CW + 2u * TS * 16) * sizeof(T);
+  constexpr int NZ = (EPI == 2 && sizeof(T) == 2) ? NSF : 0;  // gate-input stages in the forward ring
+  constexpr uint32_t kFwdBytes = (2u * TS * CW + 2u * TS * 16 + (NZ > 0 ? TS * CW : 0u)) * sizeof(T);
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t pad = (128u - (su32(smem_raw) & 127u)) & 127u;
   R& r = reinterpret_cast<R*>(smem_raw + pad)[warp];
+  T* zr = reinterpret_cast<T*>(smem_raw + pad + NW * sizeof(R)) + warp * (NZ * TS * CW);  // after the rings
   const int64_t wid = static_cast<int64_t>(blockIdx.x) * NW + warp;
   if (wid >= p.nwarps) return;
 
   if (threadIdx.x == 0) {  // bring the copy descriptors into the descriptor cache before their first use
-    const CUtensorMap* maps[7] = {&mx, &md, &mB, &mC, &mxw, &mdw, &mBw};
+    const CUtensorMap* maps[8] = {&mx, &md, &mB, &mC, &mxw, &mdw, &mBw, &mz};
 #pragma unroll
-    for (int i = 0; i < 7; ++i) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(maps[i])) : "memory");
+    for (int i = 0; i < 8; ++i) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(maps[i])) : "memory");
   }
   if (lane == 0) {
     for (int i = 0; i < NSF; ++i) mbar_init(&r.fbar[i], 1);
@@ -825,6 +835,7 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
       tma_load(r.fd[slot], &md, col, trow, &r.fbar[slot]);
       tma_load(r.fB[slot], &mB, 0, trow, &r.fbar[slot]);
       tma_load(r.fC[slot], &mC, 0, trow, &r.fbar[slot]);
+      if constexpr (NZ > 0) tma_load(zr + slot * TS * CW, &mz, col, trow, &r.fbar[slot]);
     }
     ipos += n;
     it += n;
@@ -886,8 +897,8 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
       }
     }
     const bool alive = __all_sync(0xffffffffu, ok)
-                           ? run_piece<true, T, ZOH, CPL, TS, NSF, TSW, NSW, DX, EPI>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0)
-                           : run_piece<false, T, ZOH, CPL, TS, NSF, TSW, NSW, DX, EPI>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0);
+                           ? run_piece<true, T, ZOH, CPL, TS, NSF, TSW, NSW, DX, EPI>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0, zr)
+                           : run_piece<false, T, ZOH, CPL, TS, NSF, TSW, NSW, DX, EPI>(r, p, &mxw, &mdw, &mBw, lane, row, t0, t1, wp, issue_fwd, kiss0, zr);
     if (!alive) break;
   }
 
@@ -939,13 +950,19 @@ template <typename T, bool ZOH, int CPL, int NW, int TS, int NSF, int TSW, int N
 cudaError_t launch_cfg(const FwdArgs& a) {
   constexpr int CW = 32 * CPL;
   const bool bf16 = sizeof(T) == 2;
-  CUtensorMap mx, md, mB, mC, mxw, mdw, mBw;  // forward tiles (TS rows) and warm-up tiles (TSW rows)
+  CUtensorMap mx, md, mB, mC, mxw, mdw, mBw, mz;  // forward tiles (TS rows), warm-up tiles (TSW rows), gate
   const uint64_t rows = static_cast<uint64_t>(a.batch * a.L);
   if (!make_map(&mx, a.x, bf16, a.D, rows, CW, TS) || !make_map(&md, a.delta, bf16, a.D, rows, CW, TS) ||
       !make_map(&mB, a.B, bf16, 16, rows, 16, TS) || !make_map(&mC, a.C, bf16, 16, rows, 16, TS) ||
       !make_map(&mxw, a.x, bf16, a.D, rows, CW, TSW) || !make_map(&mdw, a.delta, bf16, a.D, rows, CW, TSW) ||
       !make_map(&mBw, a.B, bf16, 16, rows, 16, TSW))
     return cudaErrorInvalidValue;
+  constexpr int NZ = (EPI == 2 && sizeof(T) == 2) ? NSF : 0;
+  if (NZ > 0) {
+    if (!make_map(&mz, a.z, bf16, a.D, rows, CW, TS)) return cudaErrorInvalidValue;
+  } else {
+    mz = mx;  // not read
+  }
   TmaParams p;
   p.A_log = a.A_log;
   p.h0 = a.h0;
@@ -959,7 +976,7 @@ cudaError_t launch_cfg(const FwdArgs& a) {
   p.G = (a.D + CW - 1) / CW;
   p.total = a.batch * p.G * a.L;
   p.wait_ns = wait_limit_ns();
-  const size_t smem = sizeof(WarpRing<T, CPL, TS, NSF, TSW, NSW>) * NW + 128;
+  const size_t smem = sizeof(WarpRing<T, CPL, TS, NSF, TSW, NSW>) * NW + NW * NZ * TS * CW * sizeof(T) + 128;
   auto kern = scan_fwd_tma_kernel<T, ZOH, CPL, NW, TS, NSF, TSW, NSW, DX, EPI>;
   static bool attr_set[64] = {false};
   int dev = 0;
@@ -978,7 +995,7 @@ cudaError_t launch_cfg(const FwdArgs& a) {
   if (nwarps < 1) nwarps = 1;
   p.nwarps = nwarps;
   const int64_t nctas = (nwarps + NW - 1) / NW;
-  kern<<<static_cast<unsigned>(nctas), NW * 32, smem, a.stream>>>(mx, md, mB, mC, mxw, mdw, mBw, p);
+  kern<<<static_cast<unsigned>(nctas), NW * 32, smem, a.stream>>>(mx, md, mB, mC, mxw, mdw, mBw, mz, p);
   return cudaGetLastError();
 }
 
@@ -1033,6 +1050,7 @@ bool tma_path_ok(const FwdArgs& a) {
   if (a.final_state && reinterpret_cast<uintptr_t>(a.final_state) % 16 != 0) return false;
   if (a.h0 && reinterpret_cast<uintptr_t>(a.h0) % 16 != 0) return false;
   if (reinterpret_cast<uintptr_t>(a.A_log) % 16 != 0) return false;  // rows read as float4
+  if (a.z && reinterpret_cast<uintptr_t>(a.z) % 16 != 0) return false;  // bf16 gate inputs are copied as tiles
   if (a.batch * a.L > (int64_t(1) << 30)) return false;  // TMA row coordinates are 32-bit
   if (encoder() == nullptr) return false;
   return true;
