@@ -18,8 +18,8 @@
 // warm-up costs about a quarter of a full walk.
 //
 // Data movement. Per warp, a forward ring of NSF stages holds [TS steps x 32 channels] tiles of x and
-// delta and [TS x 16] tiles of B and C; a warm-up ring of NSW stages holds the x, delta, B tiles the
-// backward walk reads. Both rings are filled by cp.async.bulk.tensor (TMA) with mbarrier completion;
+// delta (and of the gate input z when the layer's gate is fused) and [TS x 16] tiles of B and C; a warm-up
+// ring of NSW stages holds the x, delta, B tiles the backward walk reads. Both rings are filled by cp.async.bulk.tensor (TMA) with mbarrier completion;
 // the forward ring is primed when a range starts, so its copies overlap the warm-up. B and C are read
 // as shared-memory broadcasts (bf16 tiles are widened to fp32 once per stage by the warp; for the
 // structured ZOH update the warp also divides B by n + 1 there, once per stage). y is stored straight to global memory (a warp writes 32 consecutive
@@ -466,9 +466,9 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
                                           int lane, int64_t row, int64_t t0, int64_t t1, WarpPipe& wp,
                                           IssueFwd& issue_fwd, int kiss0, const T* zr) {
   constexpr int CW = 32 * CPL;
-  // bf16 inputs with the gate: z comes through the forward ring (zr: this warp's NSF stages of [TS][CW]
-  // tiles); fp32 inputs load each stage's z up front from global memory (their shared memory is full).
-  constexpr bool kZs = EPI == 2 && sizeof(T) == 2;
+  // With the gate, z comes through the forward ring like x and delta (zr: this warp's NSF stages of [TS][CW]
+  // tiles): read from global memory inside the steps, each step waited for its own load.
+  constexpr bool kZs = EPI == 2;
   constexpr bool kConv = sizeof(T) == 2;  // bf16: consumers read B and C from the widened Bf / Cf
   constexpr uint32_t kWarmBytes = (2u * TSW * CW + TSW * 16) * sizeof(T);
   const int64_t L = p.L;
@@ -692,12 +692,12 @@ __device__ __forceinline__ bool run_piece(WarpRing<T, CPL, TS, NSF, TSW, NSW>& r
       constexpr bool kPipe = sizeof(T) == 4;
       if (kPipe && n == TS && full) {
         float2 e[CPL][8], s2[CPL];
-        float zt[EPI == 2 ? TS : 1][CPL];  // gate inputs of the stage, loaded up front
+        float zt[EPI == 2 ? TS : 1][CPL];  // gate inputs of the stage, from its ring tile
         if constexpr (EPI == 2) {
 #pragma unroll
           for (int i = 0; i < TS; ++i)
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) zt[i][c] = tof<T>(zp[static_cast<int64_t>(i) * p.D + 32 * c]);
+            for (int c = 0; c < CPL; ++c) zt[i][c] = tof<T>(zr[slot * TS * CW + i * CW + c * 32 + lane]);
         }
         auto prep = [&](int i, float2 (&ee)[CPL][8], float2 (&ss)[CPL]) {
           float xv[CPL], dv[CPL];
@@ -787,7 +787,7 @@ scan_fwd_tma_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constan
                     TmaParams p) {
   using R = WarpRing<T, CPL, TS, NSF, TSW, NSW>;
   constexpr int CW = R::CW;
-  constexpr int NZ = (EPI == 2 && sizeof(T) == 2) ? NSF : 0;  // gate-input stages in the forward ring
+  constexpr int NZ = EPI == 2 ? NSF : 0;  // gate-input stages in the forward ring
   constexpr uint32_t kFwdBytes = (2u * TS * CW + 2u * TS * 16 + (NZ > 0 ? TS * CW : 0u)) * sizeof(T);
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -957,7 +957,7 @@ cudaError_t launch_cfg(const FwdArgs& a) {
       !make_map(&mxw, a.x, bf16, a.D, rows, CW, TSW) || !make_map(&mdw, a.delta, bf16, a.D, rows, CW, TSW) ||
       !make_map(&mBw, a.B, bf16, 16, rows, 16, TSW))
     return cudaErrorInvalidValue;
-  constexpr int NZ = (EPI == 2 && sizeof(T) == 2) ? NSF : 0;
+  constexpr int NZ = EPI == 2 ? NSF : 0;
   if (NZ > 0) {
     if (!make_map(&mz, a.z, bf16, a.D, rows, CW, TS)) return cudaErrorInvalidValue;
   } else {
@@ -1003,6 +1003,8 @@ cudaError_t launch_cfg(const FwdArgs& a) {
 // stages. fp32 inputs: 8 warps (2 per SM sub-partition) with deeper rings; bf16 inputs (half the bytes per
 // element, so smaller rings suffice): 12 warps, whose extra latency hiding is worth 12% there.
 struct ShapeF32 { static constexpr int CPL = 2, NW = 8, TS = 8, NSF = 3, TSW = 8, NSW = 2; };
+// fp32 with the gate: the z tiles take the room of half the warm-up ring (4-step warm-up tiles)
+struct ShapeF32Gate { static constexpr int CPL = 2, NW = 8, TS = 8, NSF = 3, TSW = 4, NSW = 2; };
 struct ShapeBF16 { static constexpr int CPL = 2, NW = 12, TS = 8, NSF = 2, TSW = 4, NSW = 2; };
 #if SSM_TMA_CFG == 1  // experiment hooks: one shape for both input types
 struct ShapeAlt { static constexpr int CPL = 2, NW = 12, TS = 8, NSF = 2, TSW = 4, NSW = 2; };
@@ -1060,6 +1062,8 @@ cudaError_t launch_fwd_tma(const FwdArgs& a) {
   if (a.dtype == 1)
     return a.disc == 1 ? launch_shape<__nv_bfloat16, true, SSM_SHAPE_BF16>(a)
                        : launch_shape<__nv_bfloat16, false, SSM_SHAPE_BF16>(a);
+  if (a.z)
+    return a.disc == 1 ? launch_shape<float, true, ShapeF32Gate>(a) : launch_shape<float, false, ShapeF32Gate>(a);
   return a.disc == 1 ? launch_shape<float, true, SSM_SHAPE_F32>(a) : launch_shape<float, false, SSM_SHAPE_F32>(a);
 }
 
