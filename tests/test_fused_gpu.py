@@ -49,7 +49,7 @@ def _f32(a):
     return None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
 
 
-SHAPES = [(2, 500, 128, 16), (1, 3000, 64, 16), (1, 300, 70, 8)]  # TMA path x2, general path
+SHAPES = [(2, 500, 128, 16), (1, 3000, 64, 16), (2, 300, 96, 16), (1, 300, 70, 8)]  # TMA path x3 (D = 96: a partial channel group), general path
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"b{s[0]}_L{s[1]}_D{s[2]}_N{s[3]}" for s in SHAPES])
