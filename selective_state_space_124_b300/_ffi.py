@@ -8,7 +8,9 @@ from __future__ import annotations
 import ctypes
 import os
 
-from .build import LIB
+# the in-tree build's output (the same path build.py writes); build.py is not imported here, so that
+# `python -m selective_state_space_124_b300.build` runs it as a fresh module
+LIB = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libssm_scan.so")
 
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT = range(5)
 DTYPE = {"f32": 0, "bf16": 1}

@@ -42,10 +42,6 @@
 #include "common.cuh"
 #include "launch.h"
 
-#ifndef SSM_TMA_CFG
-#define SSM_TMA_CFG 0
-#endif
-
 namespace ssm {
 
 __device__ int g_device_status = 0;  // nonzero: a bounded wait ran out (read by ssm_check_device)
@@ -1006,18 +1002,6 @@ struct ShapeF32 { static constexpr int CPL = 2, NW = 8, TS = 8, NSF = 3, TSW = 8
 // fp32 with the gate: the z tiles take the room of half the warm-up ring (4-step warm-up tiles)
 struct ShapeF32Gate { static constexpr int CPL = 2, NW = 8, TS = 8, NSF = 3, TSW = 4, NSW = 2; };
 struct ShapeBF16 { static constexpr int CPL = 2, NW = 12, TS = 8, NSF = 2, TSW = 4, NSW = 2; };
-#if SSM_TMA_CFG == 1  // experiment hooks: one shape for both input types
-struct ShapeAlt { static constexpr int CPL = 2, NW = 12, TS = 8, NSF = 2, TSW = 4, NSW = 2; };
-#define SSM_SHAPE_F32 ShapeAlt
-#define SSM_SHAPE_BF16 ShapeAlt
-#elif SSM_TMA_CFG == 2
-struct ShapeAlt { static constexpr int CPL = 2, NW = 8, TS = 8, NSF = 3, TSW = 8, NSW = 2; };
-#define SSM_SHAPE_F32 ShapeAlt
-#define SSM_SHAPE_BF16 ShapeAlt
-#else
-#define SSM_SHAPE_F32 ShapeF32
-#define SSM_SHAPE_BF16 ShapeBF16
-#endif
 
 template <typename T, bool ZOH, typename S, int DX, int EPI>
 cudaError_t launch_fused(const FwdArgs& a) {
@@ -1060,11 +1044,11 @@ bool tma_path_ok(const FwdArgs& a) {
 
 cudaError_t launch_fwd_tma(const FwdArgs& a) {
   if (a.dtype == 1)
-    return a.disc == 1 ? launch_shape<__nv_bfloat16, true, SSM_SHAPE_BF16>(a)
-                       : launch_shape<__nv_bfloat16, false, SSM_SHAPE_BF16>(a);
+    return a.disc == 1 ? launch_shape<__nv_bfloat16, true, ShapeBF16>(a)
+                       : launch_shape<__nv_bfloat16, false, ShapeBF16>(a);
   if (a.z)
     return a.disc == 1 ? launch_shape<float, true, ShapeF32Gate>(a) : launch_shape<float, false, ShapeF32Gate>(a);
-  return a.disc == 1 ? launch_shape<float, true, SSM_SHAPE_F32>(a) : launch_shape<float, false, SSM_SHAPE_F32>(a);
+  return a.disc == 1 ? launch_shape<float, true, ShapeF32>(a) : launch_shape<float, false, ShapeF32>(a);
 }
 
 int read_and_clear_device_status() {

@@ -31,6 +31,10 @@ def test_every_declared_symbol_is_exported(lib):
         assert s in _ffi.SIGNATURES, f"{s} has no ctypes signature in the binding"
 
 
+def test_binding_loads_the_library_the_build_writes():
+    assert _ffi.LIB == build.LIB
+
+
 def test_version_and_status_strings(lib):
     assert lib.ssm_version() >= 100
     for code, name in enumerate(["SSM_OK", "SSM_ERR_INVALID_ARG", "SSM_ERR_UNSUPPORTED", "SSM_ERR_CUDA",
