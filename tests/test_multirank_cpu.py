@@ -89,3 +89,14 @@ def test_compulsory_byte_and_flop_counts():
     assert bench.ssd_flops(ssd) == 2 * 128 * 128 * 64 + 2 * (2 * 128 * 128 * 16 + 4 * 128 * 64 * 16)
     # one chunk of Q = 64 (the warp-MMA kernel's chunk length)
     assert bench.ssd_flops(ssd, Q=64) == 2 * 64 * 64 * 64 + 2 * (2 * 64 * 64 * 16 + 4 * 64 * 64 * 16)
+
+
+def test_committed_traffic_matches_the_current_prefill_sources():
+    """profiles/ncu_traffic.json was captured on the prefill kernel as it stands (same source hash), so the
+    bench line's roofline.traffic is not null; a record for another kernel is not used."""
+    import bench
+    for name in ("long", "mamba130m", "mamba1p4b"):
+        t = bench.ncu_traffic("scan_fwd", name)
+        assert t is not None and t > 0, name
+    assert bench.ncu_traffic("scan_bwd", "long") is None
+    assert bench.ncu_traffic("scan_fwd", "no_such_workload") is None
