@@ -11,8 +11,9 @@ after it and reported under "workloads".
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 Timing: W untimed steps, then K timed steps bracketed by a barrier and a device synchronise; L2 is
-flushed (a 512 MiB write) before every step, outside the CUDA-event pairs that time the step's kernels
-on the launching stream; the job time is the maximum over ranks. Multi-GPU runs (torchrun) are weak
+flushed (a 512 MiB write, then a read of the same buffer, so that no dirty line of the flush is left to
+write back) before every step, outside the CUDA-event pairs that time the step's kernels on the launching
+stream; the job time is the maximum over ranks. Multi-GPU runs (torchrun) are weak
 scaling: every rank scans its own independent batch on its own GPU, with no data-path collective.
 
 --impl reference times the CPU oracle (double precision, OpenMP over channels, as it stands) on the
@@ -106,6 +107,14 @@ def bwd_bytes(cfg):
     es = 2 if cfg["dtype"] == "bf16" else 4
     b, L, D, N = cfg["batch"], cfg["L"], cfg["D"], cfg["N"]
     return 5 * b * L * D * es + 2 * b * L * N * es + 2 * b * L * N * 4 + 2 * D * N * 4 + b * D * N * 4
+
+
+def flush_l2(buf):
+    """Evict the L2 before a timed launch: write a buffer larger than the L2 (126 MB), then read it back. The
+    read leaves only clean lines in the L2, so the timed kernels do not also pay for writing the flush's own
+    data back to DRAM (about 100 MB of dirty lines after the write alone)."""
+    buf.zero_()
+    buf.sum()
 
 
 def step_bytes(cfg):
@@ -287,7 +296,7 @@ def measure_prefill(name, reps, flush, peak, fused=False):
         launch = lambda: lib.ssm_scan_fwd_ptr(*args)
     ms = []
     for i in range(3 + reps):
-        flush.zero_()
+        flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         launch()
@@ -338,7 +347,7 @@ def measure_backward(name, reps, flush, peak):
              v(stream.cuda_stream))
     ms = []
     for i in range(3 + reps):
-        flush.zero_()
+        flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         _ffi.check("ssm_scan_bwd", fn(*cargs))
@@ -398,7 +407,7 @@ def measure_ssd(name, reps, flush, peak):
                                                                  _ffi.DISC[cfg["disc"]], ctypes.c_void_p(stream.cuda_stream)]
     ms = []
     for i in range(3 + reps):
-        flush.zero_()
+        flush_l2(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         _ffi.check("ssm_ssd_fwd", fn(*cargs))
@@ -459,7 +468,7 @@ def measure_decode(steps, flush, peak):
     stream = torch.cuda.current_stream()
     ms = []
     for i in range(3 + 50):
-        flush.zero_()
+        flush_l2(flush)
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
         lib.ssm_scan_step_ptr(*step_args(i, stream))
@@ -555,7 +564,7 @@ def workload_config(args, world):
     es = 2 if cfg["dtype"] == "bf16" else 4
     in_bytes = cfg["batch"] * cfg["L"] * (2 * cfg["D"] + 2 * cfg["N"]) * es
     config = {"workload": describe(args.workload, cfg),
-              "l2": f"L2 flushed (512 MiB write) before every step; prefill inputs {in_bytes / 1e9:.3g} GB "
+              "l2": f"L2 flushed (512 MiB write, then read back) before every step; prefill inputs {in_bytes / 1e9:.3g} GB "
                     f"({'larger' if in_bytes > 126e6 else 'smaller'} than the 126 MB L2)",
               "parallelism": f"weak x{world}: one independent batch per GPU (seed = rank), no collective"}
     return overrides, cfg, config
@@ -681,7 +690,7 @@ def main(argv=None):
         lib.ssm_scan_step_ptr(*step_args)
 
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush_l2(flush)
         fwd()
         step()
     lib.check_device()
@@ -697,7 +706,7 @@ def main(argv=None):
         wall0 = time.perf_counter()
         head.zero_()  # a long first write: the host enqueues ahead of the device from the start
         for i in range(K):
-            flush.zero_()
+            flush_l2(flush)
             ev[i][0].record(stream)
             fwd()
             ev[i][1].record(stream)
@@ -734,7 +743,7 @@ def main(argv=None):
             dist.barrier()
         torch.cuda.synchronize()
         for i in range(KE):
-            flush.zero_()
+            flush_l2(flush)
             eve[i][0].record(stream)
             lib.ssm_scan_fwd_host(hx["x"], hx["delta"], hx["A_log"], hx["B"], hx["C"], disc=cfg["disc"], y=hy,
                                   final_state=hs, workspace=hws, stream=stream, seg_L=seg)

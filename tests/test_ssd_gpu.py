@@ -142,6 +142,30 @@ def test_ssd_six_heads_per_cta_zoh_h0_sampled_heads(orc):
     assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
 
 
+def test_ssd_odd_heads_several_waves_sampled_heads(orc):
+    """An odd head count at a size whose chunk-state grid takes several waves (batch 1, L 8100: 64 chunks, the
+    last of 36 steps; 29 heads x 64, N 128: 960 head-pair CTAs), so the last pair of every chunk has one head.
+    The oracle on four heads: the first, an inner one, the last full pair's second head and the unpaired last
+    head, every step and state entry."""
+    import torch
+    import selective_state_space_124_b300 as lib
+    batch, L, H, P, N = 1, 8100, 29, 64, 128
+    inp = ssm_inputs.make_ssd_inputs(batch, L, H, P, N, seed=29)
+    x = _bf16(torch, inp["x_bits"], (batch, L, H, P))
+    B = _bf16(torch, inp["B_bits"], (batch, L, N))
+    C = _bf16(torch, inp["C_bits"], (batch, L, N))
+    y, fs = lib.ssm_ssd_fwd(x, torch.from_numpy(inp["delta"]).cuda(), torch.from_numpy(inp["A_log"]).cuda(), B, C,
+                            disc="euler")
+    lib.check_device()
+    heads = [0, 6, 27, 28]
+    yr, sr = orc.ssd_fwd(np.ascontiguousarray(inp["x"][:, :, heads]), np.ascontiguousarray(inp["delta"][:, :, heads]),
+                         inp["A_log"][heads], inp["B"], inp["C"], disc="euler")
+    ey = rel_err(y[:, :, heads].float().cpu().numpy(), yr)
+    es = rel_err(fs[:, heads].cpu().numpy(), sr)
+    assert ey <= TOL["bf16"], f"y rel err {ey:.3g}"
+    assert es <= TOL["bf16"], f"final state rel err {es:.3g}"
+
+
 def test_ssd_rejects_unsupported_shapes():
     import torch
     import selective_state_space_124_b300 as lib
