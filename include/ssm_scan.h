@@ -34,6 +34,11 @@
  *  - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = the legacy default
  *    stream) and runs asynchronously; the return code covers argument checks and launch errors.
  *    ssm_check_device() synchronises the stream and reports errors raised while kernels ran.
+ *  - Apart from ssm_check_device (which synchronises) and ssm_scan_fwd_host (which also uses streams of
+ *    its own), a call only launches kernels on `stream`. After a first call on a device (which sets kernel
+ *    attributes once), the calls can therefore be captured into a CUDA graph and replayed; and calls on
+ *    different streams need no ordering between them, except ssm_scan_bwd_noalloc, whose scratch array
+ *    is shared by all its calls on a device.
  *  - For the diagonal scan, N (state size) must be in [1, 16]; larger N returns SSM_ERR_UNSUPPORTED. The
  *    SSD layer has its own sizes (see ssm_ssd_fwd).
  *  - Outputs may not overlap inputs (checked on the pointer ranges: SSM_ERR_INVALID_ARG).
